@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark: ring all-reduce of N virtual ranks on one GB300.
+
+Default workload: 8 ranks x 64 Mi fp32 elements (256 MiB per rank), op avg,
+per-rank seeded normal(0, 1e-3) gradients. One step = one ra_allreduce call
+(one fused kernel launch) over inputs already resident in HBM. The metric is
+the all-reduce algorithm bandwidth S/t (S = bytes per rank), aggregated over
+GPUs when run as replicas under torchrun; the roofline block gives the HBM
+fraction of the algorithmic traffic 2*N*S per launch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py --sweep OUT.jsonl      # message-size sweep, one line per (N, size, call)
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ring_all_reduce_02_gb300 import inputs  # noqa: E402
+
+METRIC = "all-reduce algorithm GB/s and % of HBM roofline vs message size, N=8 ranks, 1 GPU"
+DEFAULT_WORKLOAD = "ar_n8_f32_avg_64m"
+GB = 1e9
+
+
+# ---------------------------------------------------------------------------
+# environment: ranks, peaks, clocks
+# ---------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []  # (t, sm_mhz, max_mhz, reasons[list])
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, mx = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(names, f[5:9]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, mx, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for s in self.samples if t0 - 0.15 <= s[0] <= t1 + 0.15]
+        used = inside if len(inside) >= 2 else self.samples
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({r for s in used for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in used), "sm_max_mhz": max(s[2] for s in used),
+                "reasons": reasons, "samples": len(used), "in_timed_region": len(inside)}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ring_all_reduce_02_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    p = os.path.join(ROOT, "profiles", f"ar_fused_kernel__{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    with open(p) as f:
+        for ln in f:
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha256_16") != kernel_source_sha():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as a baseline (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+def oracle_rate(n, length, dtype, op, dist, target_s: float, max_len: int):
+    """Time the oracle on a sample of the workload sized to about target_s; returns (GB/s, sample_len, secs)."""
+    import oracle
+
+    oracle.build()
+    probe = min(max_len, 1 << 20)
+    xs = inputs.rank_buffers(n, probe, dtype, dist)
+    t = time.perf_counter()
+    oracle.allreduce(xs, op, dtype)
+    dt = max(time.perf_counter() - t, 1e-4)
+    sample = int(min(max_len, max(4096 * n, probe * target_s / dt)))
+    xs = inputs.rank_buffers(n, sample, dtype, dist)
+    t = time.perf_counter()
+    oracle.allreduce(xs, op, dtype)
+    dt = time.perf_counter() - t
+    s_bytes = sample * inputs.ELEM_SIZE[dtype]
+    return s_bytes / dt / GB, sample, dt
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    n, length, dtype, op, dist = inputs.WORKLOADS[args.workload]
+    import oracle
+
+    oracle.build()
+    # size each step so warm-up + timed steps take about a minute in total
+    _, sample, _ = oracle_rate(n, length, dtype, op, dist, target_s=min(5.0, 60.0 / max(1, args.steps + args.warmup)),
+                               max_len=length)
+    xs = inputs.rank_buffers(n, sample, dtype, dist)
+    for _ in range(args.warmup):
+        oracle.allreduce(xs, op, dtype)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.allreduce(xs, op, dtype)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    s_bytes = sample * inputs.ELEM_SIZE[dtype]
+    value = s_bytes * args.steps / total / GB
+    cores = min(n, os.cpu_count() or 1)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": config_block(args.workload),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} ranks x {sample} {dtype} elements per step (the workload is {length})"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(workload: str):
+    n, length, dtype, op, dist = inputs.WORKLOADS[workload]
+    s_bytes = length * inputs.ELEM_SIZE[dtype]
+    return {"workload": workload, "nranks": n, "count": length, "dtype": dtype, "op": op,
+            "bytes_per_rank": s_bytes, "inputs": f"seeded {dist[0]}{tuple(dist[1:])}, seed = rank",
+            "l2": f"inputs larger than L2 ({2 * n * s_bytes / GB:.1f} GB touched per step vs ~0.13 GB L2)",
+            "parallelism": "replicas (one N-rank instance per GPU)"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from ring_all_reduce_02_gb300 import build, ra
+
+    build.build()
+    ra.lib()
+    dev = torch.cuda.current_device()
+    n, length, dtype, op, dist_spec = inputs.WORKLOADS[args.workload]
+    es = inputs.ELEM_SIZE[dtype]
+    s_bytes = length * es
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "i32": torch.int32}[dtype]
+
+    host = inputs.rank_buffers(n, length, dtype, dist_spec)
+    pinned_in, sends = [], []
+    for x in host:
+        t = torch.from_numpy(x.view(np.int16) if dtype == "bf16" else x)
+        p = t.pin_memory()
+        pinned_in.append(p.view(tdt) if dtype == "bf16" else p)
+        sends.append(pinned_in[-1].to(f"cuda:{dev}"))
+    del host
+    recvs = [torch.empty_like(s) for s in sends]
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        ra.ra_allreduce(sends, recvs, op, stream=stream)
+    sampler = ClockSampler(dev).start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    t_wall0 = time.time()
+    for k in range(args.steps):
+        starts[k].record(stream)
+        ra.ra_allreduce(sends, recvs, op, stream=stream)
+        ends[k].record(stream)
+    barrier()
+    t_wall1 = time.time()
+    launches = args.steps  # one fused kernel per call
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms, per launch
+    total_ms = starts[0].elapsed_time(ends[-1])
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=f"cuda:{dev}")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    ms_per_step = total_ms / args.steps
+    value = world * s_bytes / (ms_per_step * 1e-3) / GB
+    avg_launch_ms = sum(per) / len(per)
+    peak, peak_kind = measured_peaks()
+    achieved = 2 * n * s_bytes / (avg_launch_ms * 1e-3) / GB
+    traffic = profiled_traffic(args.workload)
+
+    # end to end through the public call with host buffers: pinned host -> device copies of
+    # every rank's input, the all-reduce, device -> pinned host copies of every rank's result
+    e2e_steps = max(3, min(args.steps, 20))
+    pinned_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in recvs]
+    for _ in range(2):
+        for p, s in zip(pinned_in, sends):
+            s.copy_(p, non_blocking=True)
+        ra.ra_allreduce(sends, recvs, op, stream=stream)
+        for p, r in zip(pinned_out, recvs):
+            p.copy_(r, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for p, s in zip(pinned_in, sends):
+            s.copy_(p, non_blocking=True)
+        ra.ra_allreduce(sends, recvs, op, stream=stream)
+        for p, r in zip(pinned_out, recvs):
+            p.copy_(r, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device=f"cuda:{dev}")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * s_bytes / (e2e_ms * 1e-3) / GB
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, sample, secs = oracle_rate(n, length, dtype, op, dist_spec, target_s=10.0, max_len=length)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": min(n, os.cpu_count() or 1), "kind": "oracle",
+               "sample": f"{n} ranks x {sample} {dtype} elements ({secs:.1f} s, one thread per rank)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": config_block(args.workload),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "ar_fused_kernel", "algorithmic_bytes_per_launch": 2 * n * s_bytes,
+                         "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                         "launch_ms": {"mean": round(avg_launch_ms, 5), "min": round(min(per), 5),
+                                       "median": round(statistics.median(per), 5)}},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": n * s_bytes,
+                    "d2h_bytes_per_step": n * s_bytes, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# message-size sweep (not the headline line): AR / RS / AG timed separately
+# ---------------------------------------------------------------------------
+def run_sweep(args):
+    import torch
+
+    from ring_all_reduce_02_gb300 import build, ra
+
+    build.build()
+    torch.cuda.set_device(0)
+    peak, peak_kind = measured_peaks()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(int(2 * l2), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    out = open(args.sweep, "w")
+    for (n, length, dtype, op, dist_spec) in inputs.size_sweep():
+        if args.sweep_max and length > args.sweep_max:
+            continue
+        es = inputs.ELEM_SIZE[dtype]
+        s_bytes = length * es
+        g = torch.Generator(device="cuda")
+        g.manual_seed(0)
+        sends = [torch.empty(length, dtype=torch.float32, device="cuda").uniform_(-1, 1, generator=g) for _ in range(n)]
+        recvs = [torch.empty_like(s) for s in sends]
+        bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+        shards = [torch.empty(e - b, dtype=torch.float32, device="cuda") for b, e in bounds]
+        calls = {
+            "allreduce": (lambda: ra.ra_allreduce(sends, recvs, op, stream=stream), 2 * n * s_bytes),
+            "reduce_scatter": (lambda: ra.ra_reduce_scatter(sends, shards, op, stream=stream), (n + 1) * s_bytes),
+            "allgather": (lambda: ra.ra_allgather(shards, recvs, stream=stream), (n + 1) * s_bytes),
+        }
+        for name, (fn, hbm_bytes) in calls.items():
+            resident = hbm_bytes < l2
+            for _ in range(5):
+                fn()
+            reps = 20
+            times = []
+            for _ in range(reps):
+                if not resident:
+                    flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                times.append(a.elapsed_time(b) * 1e-3)
+            rec = {"call": name, "nranks": n, "bytes_per_rank": s_bytes, "count": length,
+                   "median_us": round(1e6 * statistics.median(times), 3), "min_us": round(1e6 * min(times), 3),
+                   "algbw_GBps": round(s_bytes / statistics.median(times) / GB, 3),
+                   "hbm_GBps": round(hbm_bytes / statistics.median(times) / GB, 1),
+                   "hbm_frac": None if resident else round(hbm_bytes / statistics.median(times) / GB / peak, 4),
+                   "l2_resident": resident, "peak": f"{peak} ({peak_kind})"}
+            if resident:
+                # warm, back-to-back launches captured in one CUDA graph: launch cost amortised
+                gs = torch.cuda.Stream()
+                gs.wait_stream(stream)
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(gs):
+                    fn_g = {"allreduce": lambda: ra.ra_allreduce(sends, recvs, op, stream=gs),
+                            "reduce_scatter": lambda: ra.ra_reduce_scatter(sends, shards, op, stream=gs),
+                            "allgather": lambda: ra.ra_allgather(shards, recvs, stream=gs)}[name]
+                    fn_g()
+                    torch.cuda.synchronize()
+                    with torch.cuda.graph(graph, stream=gs):
+                        for _ in range(100):
+                            fn_g()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                graph.replay()
+                torch.cuda.synchronize()
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                rec["graph_us_per_call"] = round(1e3 * a.elapsed_time(b) / 100, 3)
+            out.write(json.dumps(rec) + "\n")
+            out.flush()
+            print(json.dumps(rec), flush=True)
+        del sends, recvs, shards
+        torch.cuda.empty_cache()
+    out.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")
+    ap.add_argument("--sweep-max", type=int, default=0, help="largest count in the sweep (0 = all)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,137 @@
+/*
+ * ra.h — C ABI of the GB300 ring all-reduce library (libra.so).
+ *
+ * N "virtual ranks" live in one GPU's memory; each rank r owns a send buffer
+ * and a receive buffer (device pointers). The calls follow the shape of
+ * ncclAllReduce(sendbuff, recvbuff, count, datatype, op, comm, stream) as the
+ * arjunsriva.com page "AllReduce, All the Way Down" (section "The Contract:
+ * What AllReduce Means") states it, with the communicator replaced by
+ * `nranks` and one host array of N device pointers per side.
+ *
+ * What is computed (tirogla.com "Ring all-reduce", section "How it works"):
+ * the buffer of `count` elements is cut into N chunks, chunk c covering
+ * elements [c*count/N, (c+1)*count/N) with floor division (section "Code"), so
+ * chunks may differ by one element and may be empty. Element i of chunk c is
+ * reduced in ring order, left to right,
+ *
+ *     x_c (+) x_{c+1} (+) ... (+) x_{c+N-1}      (rank indices mod N)
+ *
+ * which is the order in which the reduce-scatter phase of the ring visits
+ * chunk c (it starts at rank c and ends at rank c-1, which then owns it).
+ * Every hop is rounded to the buffer dtype: fp32 hops are fp32 operations;
+ * fp16/bf16 hops compute in fp32 and round to nearest even once; int32 sum and
+ * prod wrap modulo 2^32. RA_AVG is the ring sum followed by one multiply by
+ * 1.0f/N (fp32) rounded to the dtype (int32: wrapped sum / N, truncated).
+ * RA_MIN / RA_MAX follow IEEE 754-2019 minimum / maximum (NaN propagates,
+ * -0 < +0). Results are bit-identical on every rank (same page,
+ * "Implementation notes").
+ *
+ * Common rules for the three collectives:
+ *  - count is the FULL per-rank vector length L in every call (also for
+ *    reduce-scatter and all-gather, whose compact side holds one chunk).
+ *  - sendbufs / recvbufs are host arrays of `nranks` device pointers. The
+ *    arrays are read during the call only; the device buffers belong to the
+ *    caller and must stay alive until the work on `stream` has completed.
+ *  - The library allocates nothing and keeps no state between calls; calls
+ *    are reentrant. Work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and the call returns without waiting.
+ *  - Arguments are checked on the host before any launch; on any error
+ *    nothing is enqueued. Every pointer must be aligned to the element size;
+ *    a pointer to a zero-length buffer may be NULL. Any other alignment is
+ *    accepted: the 16-byte vector path is used when the buffers share their
+ *    address modulo 16, a per-element path otherwise.
+ *  - Buffers must not overlap, except in the exact in-place layout named for
+ *    each call (each element is then read and written by the same thread).
+ *    Send buffers may overlap each other (they are only read).
+ *  - count == 0 returns RA_SUCCESS and launches nothing. nranks == 1 copies.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RA_MAX_RANKS 64
+/* largest accepted count: keeps c*count (c <= 64) inside 63 bits */
+#define RA_MAX_COUNT ((((uint64_t)1) << 57) - 1)
+
+typedef enum {
+  RA_SUCCESS = 0,
+  RA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, nranks outside [1, 64], bad enum, count too big */
+  RA_ERR_UNSUPPORTED = 2, /* a dtype/op pair this build does not provide */
+  RA_ERR_ALIAS = 3,       /* buffers overlap other than in the allowed in-place layout */
+  RA_ERR_CUDA = 4         /* the CUDA launch failed; see ra_last_cuda_error() */
+} ra_status_t;
+
+typedef enum { RA_FLOAT32 = 0, RA_FLOAT16 = 1, RA_BFLOAT16 = 2, RA_INT32 = 3 } ra_dtype_t;
+
+/* bitfern.com "AllReduce Explained", section "What Is AllReduce?": sum,
+ * average, minimum, maximum and product reductions. */
+typedef enum { RA_SUM = 0, RA_AVG = 1, RA_MIN = 2, RA_MAX = 3, RA_PROD = 4 } ra_op_t;
+
+/*
+ * All-reduce (tirogla.com "Ring all-reduce", "How it works": reduce-scatter
+ * then all-gather). sendbufs[r]: count elements of rank r. recvbufs[r]: count
+ * elements; on completion every recvbufs[r] holds the reduction of all ranks.
+ * In place: recvbufs[r] == sendbufs[r].
+ * HBM traffic: reads N*count*e bytes, writes N*count*e bytes, in one launch.
+ */
+ra_status_t ra_allreduce(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                         ra_dtype_t dtype, ra_op_t op, int nranks, void* stream);
+
+/*
+ * Reduce-scatter (infra-guide "Collective communication primitives", section
+ * 3.5: rank i keeps reduced shard i). sendbufs[r]: count elements.
+ * recvbufs[r]: chunk r only, (end_r - begin_r) elements, compact. The shard
+ * is reduced in the same ring order as ra_allreduce, so the all-gather of
+ * these shards equals ra_allreduce bit for bit (same page, section 3.8).
+ * In place: recvbufs[r] == sendbufs[r] + begin_r elements.
+ * HBM traffic: reads N*count*e, writes count*e.
+ */
+ra_status_t ra_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                              ra_dtype_t dtype, ra_op_t op, int nranks, void* stream);
+
+/*
+ * All-gather (ramchalamkr.github.io "NCCL Primitives Deep Dive", section 1;
+ * infra-guide section 3.6). sendbufs[r]: chunk r, (end_r - begin_r) elements,
+ * compact. recvbufs[r]: count elements; on completion each holds every chunk
+ * at its place. `op` is ignored (no reduction happens).
+ * In place: sendbufs[r] == recvbufs[r] + begin_r elements.
+ * HBM traffic: reads count*e, writes N*count*e.
+ */
+ra_status_t ra_allgather(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                         ra_dtype_t dtype, ra_op_t op, int nranks, void* stream);
+
+/*
+ * Chunk bounds (tirogla.com "Ring all-reduce", section "Code"):
+ * *begin = c*count/nranks, *end = (c+1)*count/nranks, floor division, exact
+ * for every count <= RA_MAX_COUNT. Host only; touches no GPU.
+ */
+ra_status_t ra_chunk_range(size_t count, int nranks, int c, size_t* begin, size_t* end);
+
+/*
+ * Planner introspection (host only, no GPU): how chunk c is split between the
+ * 16-byte vector path and the per-element path for buffers whose common
+ * address phase (address mod 16) is `phase_bytes` and whose elements are
+ * `elem_size` bytes. Writes [vec_begin, vec_end) (elements handled as 16-byte
+ * vectors; empty if vec_begin == vec_end) inside [begin, end); the elements of
+ * the chunk outside it take the per-element path.
+ */
+ra_status_t ra_plan_chunk(size_t count, int nranks, int c, int elem_size, int phase_bytes,
+                          size_t* begin, size_t* end, size_t* vec_begin, size_t* vec_end);
+
+/* A static, human-readable name for a status code. */
+const char* ra_status_string(ra_status_t status);
+
+/* The cudaError_t of the last RA_ERR_CUDA returned on the calling thread (0 if none). */
+int ra_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

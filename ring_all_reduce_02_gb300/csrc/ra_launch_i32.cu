@@ -1,0 +1,9 @@
+// Kernel instantiations for one dtype (compiled as its own translation unit so
+// the four dtypes build in parallel).
+#include "ra_kernels.cuh"
+
+namespace ra {
+cudaError_t launch_i32(int kind, int op, const Args& a, dim3 grid, cudaStream_t s) {
+  return launch_dtype<DT_I32>(kind, op, a, grid, s);
+}
+}  // namespace ra

@@ -1,0 +1,165 @@
+"""Python binding of libra.so: argument marshalling only.
+
+The functions carry the C ABI's names (include/ra.h). Tensors supply device
+pointers (``data_ptr()``) and the stream is torch's current CUDA stream unless
+one is given; every step of the collective runs in the library's kernels.
+The library must be built (``python -m ring_all_reduce_02_gb300.build``); if
+it is missing, the first call raises instead of falling back to anything.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libra.so")
+
+RA_SUCCESS, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_ALIAS, RA_ERR_CUDA = range(5)
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
+OP_CODES = {"sum": 0, "avg": 1, "min": 2, "max": 3, "prod": 4}
+RA_MAX_RANKS = 64
+
+# every symbol include/ra.h declares
+EXPORTS = ("ra_allreduce", "ra_reduce_scatter", "ra_allgather", "ra_chunk_range", "ra_plan_chunk",
+           "ra_status_string", "ra_last_cuda_error")
+
+
+class RaError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        name = lib().ra_status_string(status).decode()
+        extra = f" (cudaError {lib().ra_last_cuda_error()})" if status == RA_ERR_CUDA else ""
+        super().__init__(f"{call}: {name}{extra}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m ring_all_reduce_02_gb300.build` (no fallback exists)")
+            L = ctypes.CDLL(LIB_PATH)
+            VP, SZ, I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+            PP = ctypes.POINTER(ctypes.c_void_p)
+            PSZ = ctypes.POINTER(ctypes.c_size_t)
+            for name in ("ra_allreduce", "ra_reduce_scatter", "ra_allgather"):
+                f = getattr(L, name)
+                f.argtypes = [PP, PP, SZ, I, I, I, VP]
+                f.restype = I
+            L.ra_chunk_range.argtypes = [SZ, I, I, PSZ, PSZ]
+            L.ra_chunk_range.restype = I
+            L.ra_plan_chunk.argtypes = [SZ, I, I, I, I, PSZ, PSZ, PSZ, PSZ]
+            L.ra_plan_chunk.restype = I
+            L.ra_status_string.argtypes = [I]
+            L.ra_status_string.restype = ctypes.c_char_p
+            L.ra_last_cuda_error.argtypes = []
+            L.ra_last_cuda_error.restype = I
+            _lib = L
+    return _lib
+
+
+def ptr_array(ptrs) -> ctypes.Array:
+    return (ctypes.c_void_p * len(ptrs))(*[int(p) if p else None for p in ptrs])
+
+
+def dtype_code(t) -> int:
+    import torch
+
+    codes = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(tensors, what):
+    dt = tensors[0].dtype
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError(f"{what}: every buffer must be a CUDA tensor")
+        if t.dtype != dt:
+            raise ValueError(f"{what}: all buffers must share one dtype")
+        if not t.is_contiguous():
+            raise ValueError(f"{what}: buffers must be contiguous")
+
+
+def call(name: str, send_ptrs, recv_ptrs, count: int, dtype: int, op: int, nranks: int, stream: int) -> int:
+    """Raw C call with integer device pointers; returns the ra_status_t."""
+    f = getattr(lib(), name)
+    return f(ptr_array(send_ptrs), ptr_array(recv_ptrs), count, dtype, op, nranks, ctypes.c_void_p(stream or None))
+
+
+def ra_allreduce(sendbufs, recvbufs, op: str = "sum", stream=None) -> None:
+    """All-reduce of N equal-length tensors into N tensors (recv may be send: in place)."""
+    _check(list(sendbufs) + list(recvbufs), "ra_allreduce")
+    count = sendbufs[0].numel()
+    if any(t.numel() != count for t in list(sendbufs) + list(recvbufs)) or len(recvbufs) != len(sendbufs):
+        raise ValueError("ra_allreduce: N send and N recv buffers of one length")
+    st = call("ra_allreduce", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
+              dtype_code(sendbufs[0]), OP_CODES[op], len(sendbufs), _stream_ptr(stream))
+    if st:
+        raise RaError(st, "ra_allreduce")
+
+
+def ra_reduce_scatter(sendbufs, recvbufs, op: str = "sum", stream=None) -> None:
+    """Reduce-scatter: recvbufs[r] receives chunk r (compact) of the reduction."""
+    _check(list(sendbufs) + [t for t in recvbufs if t.numel()], "ra_reduce_scatter")
+    count, n = sendbufs[0].numel(), len(sendbufs)
+    for r, t in enumerate(recvbufs):
+        b, e = ra_chunk_range(count, n, r)
+        if t.numel() != e - b:
+            raise ValueError(f"ra_reduce_scatter: recvbufs[{r}] must hold {e - b} elements")
+    st = call("ra_reduce_scatter", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
+              dtype_code(sendbufs[0]), OP_CODES[op], n, _stream_ptr(stream))
+    if st:
+        raise RaError(st, "ra_reduce_scatter")
+
+
+def ra_allgather(sendbufs, recvbufs, stream=None) -> None:
+    """All-gather: sendbufs[r] is chunk r (compact); every recvbufs[r] receives all chunks."""
+    _check([t for t in sendbufs if t.numel()] + list(recvbufs), "ra_allgather")
+    count, n = recvbufs[0].numel(), len(recvbufs)
+    for r, t in enumerate(sendbufs):
+        b, e = ra_chunk_range(count, n, r)
+        if t.numel() != e - b:
+            raise ValueError(f"ra_allgather: sendbufs[{r}] must hold {e - b} elements")
+    st = call("ra_allgather", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
+              dtype_code(recvbufs[0]), OP_CODES["sum"], n, _stream_ptr(stream))
+    if st:
+        raise RaError(st, "ra_allgather")
+
+
+def ra_chunk_range(count: int, nranks: int, c: int) -> tuple[int, int]:
+    b, e = ctypes.c_size_t(), ctypes.c_size_t()
+    st = lib().ra_chunk_range(count, nranks, c, ctypes.byref(b), ctypes.byref(e))
+    if st:
+        raise RaError(st, "ra_chunk_range")
+    return b.value, e.value
+
+
+def ra_plan_chunk(count: int, nranks: int, c: int, elem_size: int, phase_bytes: int):
+    """(begin, end, vec_begin, vec_end) of chunk c: which part takes the 16-byte vector path."""
+    out = [ctypes.c_size_t() for _ in range(4)]
+    st = lib().ra_plan_chunk(count, nranks, c, elem_size, phase_bytes, *[ctypes.byref(o) for o in out])
+    if st:
+        raise RaError(st, "ra_plan_chunk")
+    return tuple(o.value for o in out)
+
+
+def ra_status_string(status: int) -> str:
+    return lib().ra_status_string(status).decode()

@@ -1,0 +1,384 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bar: bit-exact for every dtype and op (the ring order and per-hop rounding are
+reproduced, so the tolerance is 0 ULP; any NaN equals any NaN). Small and
+medium shapes are compared element by element against the oracle's
+message-passing ring; the full-size workloads are compared on sampled elements
+(every chunk boundary +-4, the ends, 2^17 random positions) against the
+oracle's per-element definition, plus properties that hold at any size (all
+ranks byte-identical). Guard pages around every buffer ("canaries") stand in
+for a bounds checker.
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import ELEM_SIZE, TORCH_DTYPE, assert_same_bits, to_device, to_host
+from ring_all_reduce_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["f32", "f16", "bf16", "i32"]
+OPS = ["sum", "avg", "min", "max", "prod"]
+
+
+@pytest.fixture(scope="module")
+def ra():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from ring_all_reduce_02_gb300 import build, ra as binding
+
+    build.build()
+    oracle.build()
+    return binding
+
+
+def dist_for(dtype, op):
+    if dtype == "i32":
+        return ("int_uniform", -2, 2) if op == "prod" else ("int_uniform", -1000, 1000)
+    return ("normal", 1.0)
+
+
+class Padded:
+    """A device buffer with guard regions of a fixed byte pattern on both sides."""
+
+    PAD = 256  # bytes on each side
+    FILL = 0x5A
+
+    def __init__(self, numel, dtype, offset_elems=0):
+        es = ELEM_SIZE[dtype]
+        self.dtype = dtype
+        total = self.PAD * 2 + (numel + offset_elems) * es
+        self.raw = torch.full((total,), self.FILL, dtype=torch.uint8, device="cuda")
+        start = self.PAD + offset_elems * es
+        self.view = self.raw[start:start + numel * es].view(TORCH_DTYPE[dtype])
+        self.start, self.end = start, start + numel * es
+
+    def fill(self, a: np.ndarray):
+        if a.size:
+            self.view.copy_(to_device(a, self.dtype))
+
+    def canaries_intact(self) -> bool:
+        raw = self.raw.cpu().numpy()
+        return bool((raw[:self.start] == self.FILL).all() and (raw[self.end:] == self.FILL).all())
+
+
+def run_allreduce(ra, xs, op, dtype, inplace=False, offsets=None):
+    n = len(xs)
+    offsets = offsets or [0] * (2 * n)
+    sends = [Padded(x.size, dtype, offsets[r]) for r, x in enumerate(xs)]
+    for b, x in zip(sends, xs):
+        b.fill(x)
+    recvs = sends if inplace else [Padded(xs[0].size, dtype, offsets[n + r]) for r in range(n)]
+    ra.ra_allreduce([b.view for b in sends], [b.view for b in recvs], op)
+    torch.cuda.synchronize()
+    for b in sends + ([] if inplace else recvs):
+        assert b.canaries_intact(), "write outside the buffers"
+    return [to_host(b.view, dtype) for b in recvs]
+
+
+def run_reduce_scatter(ra, xs, op, dtype, inplace=False):
+    n, length = len(xs), xs[0].size
+    sends = [Padded(length, dtype) for _ in xs]
+    for b, x in zip(sends, xs):
+        b.fill(x)
+    bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+    if inplace:
+        recvs = [s.view[b:e] for s, (b, e) in zip(sends, bounds)]
+        ra.ra_reduce_scatter([s.view for s in sends], recvs, op)
+        torch.cuda.synchronize()
+        outs = [to_host(r, dtype) for r in recvs]
+        pads = sends
+    else:
+        pads = [Padded(e - b, dtype) for b, e in bounds]
+        ra.ra_reduce_scatter([s.view for s in sends], [p.view for p in pads], op)
+        torch.cuda.synchronize()
+        outs = [to_host(p.view, dtype) for p in pads]
+        pads = pads + sends
+    for p in pads:
+        assert p.canaries_intact()
+    return outs
+
+
+def run_allgather(ra, shards, length, dtype, inplace=False):
+    n = len(shards)
+    bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+    recvs = [Padded(length, dtype) for _ in range(n)]
+    if inplace:
+        sends = []
+        for r, (b, e) in enumerate(bounds):
+            v = recvs[r].view[b:e]
+            if e > b:
+                v.copy_(to_device(shards[r], dtype))
+            sends.append(v)
+        ra.ra_allgather(sends, [p.view for p in recvs])
+        pads = recvs
+    else:
+        sp = [Padded(e - b, dtype) for b, e in bounds]
+        for p, s in zip(sp, shards):
+            p.fill(s)
+        ra.ra_allgather([p.view for p in sp], [p.view for p in recvs])
+        pads = recvs + sp
+    torch.cuda.synchronize()
+    for p in pads:
+        assert p.canaries_intact()
+    return [to_host(p.view, dtype) for p in recvs]
+
+
+def check_all(ra, xs, op, dtype, what):
+    """AR, RS and AG against the oracle; AG(RS) == AR; every rank identical."""
+    length = xs[0].size
+    want, _, _ = oracle.allreduce(xs, op, dtype)
+    got = run_allreduce(ra, xs, op, dtype)
+    for r in range(len(xs)):
+        assert_same_bits(got[r], want[r], dtype, f"{what} AR rank {r}")
+    shards_want, _ = oracle.reduce_scatter(xs, op, dtype)
+    shards = run_reduce_scatter(ra, xs, op, dtype)
+    for r in range(len(xs)):
+        assert_same_bits(shards[r], shards_want[r], dtype, f"{what} RS shard {r}")
+    ag = run_allgather(ra, shards, length, dtype)
+    ag_want, _, _ = oracle.allgather(shards_want, length, dtype)
+    for r in range(len(xs)):
+        assert_same_bits(ag[r], ag_want[r], dtype, f"{what} AG rank {r}")
+        assert ag[r].tobytes() == got[0].tobytes(), f"{what}: AG(RS) != AR"
+
+
+# ---------------------------------------------------------------------------
+# the named workloads
+# ---------------------------------------------------------------------------
+def test_n4_f32_sum_4k(ra):
+    n, length, dtype, op, dist = inputs.WORKLOADS["ar_n4_f32_sum_4k"]
+    xs = inputs.rank_buffers(n, length, dtype, dist)
+    check_all(ra, xs, op, dtype, "n4 f32 sum 4k")
+
+
+@pytest.mark.parametrize("case", inputs.sweep_cases(), ids=lambda c: f"n{c[0]}-{c[2]}-{c[3]}")
+def test_op_dtype_sweep_uneven_chunks(ra, case):
+    n, length, dtype, op, dist = case
+    xs = inputs.rank_buffers(n, length, dtype, dist)
+    want, _, _ = oracle.allreduce(xs, op, dtype)
+    got = run_allreduce(ra, xs, op, dtype)
+    for r in range(n):
+        assert_same_bits(got[r], want[r], dtype, f"rank {r}")
+    shards = run_reduce_scatter(ra, xs, op, dtype)
+    shards_want, _ = oracle.reduce_scatter(xs, op, dtype)
+    for r in range(n):
+        assert_same_bits(shards[r], shards_want[r], dtype, f"RS shard {r}")
+
+
+# ---------------------------------------------------------------------------
+# every dtype x op on small and ragged shapes, several tiles, edge cases
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,op", list(itertools.product(DTYPES, OPS)))
+def test_small_and_ragged_shapes(ra, dtype, op):
+    seed = 1000
+    for n in (1, 2, 3, 4, 5, 7, 8, 16):
+        for length in (0, 1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 33, 64, 65, 100, 257, 1000, 4097):
+            xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=seed)
+            seed += 1
+            if length == 0:
+                outs = run_allreduce(ra, xs, op, dtype)
+                assert all(o.size == 0 for o in outs)
+                continue
+            check_all(ra, xs, op, dtype, f"n={n} L={length}")
+
+
+@pytest.mark.parametrize("n,length,dtype", [(8, (1 << 20) + 13, "f32"), (8, (1 << 24) + 7, "bf16"),
+                                            (3, 3 * 600_001, "f16"), (16, 5_000_011, "f32")])
+def test_many_tiles_and_trips(ra, n, length, dtype):
+    # chunks of 10^5..2*10^6 elements: several CTAs per chunk, several trips per CTA,
+    # and a ragged tail at every chunk boundary
+    for op in ("sum", "avg"):
+        xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=77)
+        want, _, _ = oracle.allreduce(xs, op, dtype)
+        got = run_allreduce(ra, xs, op, dtype)
+        for r in range(n):
+            assert_same_bits(got[r], want[r], dtype, f"{op} rank {r}")
+
+
+def test_ring_order_is_reproduced(ra):
+    # fp32: chunk c starts the fold at x_c. x_c = 1 and 2^-24 elsewhere: ties to even keep 1.0;
+    # any other starting rank gives 1 + 2^-22. Bits must match the oracle exactly.
+    n, length = 8, 8 * 1024 + 5
+    tiny = np.float32(2.0 ** -24)
+    for c in range(n):
+        b, e = oracle.chunk_range(length, n, c)
+        xs = [np.full(length, tiny, dtype=np.float32) for _ in range(n)]
+        xs[c][b:e] = 1.0
+        want, _, _ = oracle.allreduce(xs, "sum", "f32")
+        got = run_allreduce(ra, xs, "sum", "f32")
+        assert (got[0][b:e] == np.float32(1.0)).all()
+        assert_same_bits(got[3], want[3], "f32", f"chunk {c}")
+
+
+def test_special_values(ra):
+    # NaN, infinities, signed zeros, subnormals in every float dtype
+    specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-40, 6e-8, -6e-8, 1e-39, 65504.0,
+                         -65504.0, 3.4e38, 1.0, -1.0], dtype=np.float32)
+    rng = np.random.default_rng(3)
+    for dtype in ("f32", "f16", "bf16"):
+        for op in OPS:
+            n = 5
+            length = 4 * specials.size + 11
+            xs = []
+            for r in range(n):
+                v = rng.choice(specials, size=length).astype(np.float32)
+                if dtype == "f16":
+                    xs.append(v.astype(np.float16))
+                elif dtype == "bf16":
+                    xs.append(oracle.round_f32("bf16", v))
+                else:
+                    xs.append(v)
+            want, _, _ = oracle.allreduce(xs, op, dtype)
+            got = run_allreduce(ra, xs, op, dtype)
+            for r in range(n):
+                assert_same_bits(got[r], want[r], dtype, f"{dtype} {op} rank {r}")
+
+
+def test_int32_wrap_and_avg(ra):
+    n, length = 3, 1001
+    big = [np.full(length, 2**31 - 5 - r, dtype=np.int32) for r in range(n)]
+    for op in ("sum", "prod", "avg"):
+        want, _, _ = oracle.allreduce(big, op, "i32")
+        got = run_allreduce(ra, big, op, "i32")
+        assert_same_bits(got[0], want[0], "i32", op)
+
+
+# ---------------------------------------------------------------------------
+# layouts: in place, offset views, mixed phases
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_inplace_equals_out_of_place(ra, dtype):
+    n, length = 5, 1003 * 17
+    xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, "sum"), seed_base=5)
+    a = run_allreduce(ra, xs, "sum", dtype)
+    b = run_allreduce(ra, xs, "sum", dtype, inplace=True)
+    for r in range(n):
+        assert a[r].tobytes() == b[r].tobytes()
+    s1 = run_reduce_scatter(ra, xs, "sum", dtype)
+    s2 = run_reduce_scatter(ra, xs, "sum", dtype, inplace=True)
+    for r in range(n):
+        assert s1[r].tobytes() == s2[r].tobytes()
+    g1 = run_allgather(ra, s1, length, dtype)
+    g2 = run_allgather(ra, s1, length, dtype, inplace=True)
+    for r in range(n):
+        assert g1[r].tobytes() == g2[r].tobytes() == a[0].tobytes()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_offset_views(ra, dtype):
+    # every buffer at the same element offset (vector path with a head), then at different
+    # offsets (per-element path); compact sides of RS/AG at arbitrary offsets
+    n, length = 4, 10_007
+    xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=9)
+    want, _, _ = oracle.allreduce(xs, "avg", dtype)
+    es = ELEM_SIZE[dtype]
+    per_vec = 16 // es
+    for offsets in ([1] * 8, [per_vec - 1] * 8, [0, 1, 2, 3, 0, 1, 2, 3], [0] * 4 + [1] * 4):
+        got = run_allreduce(ra, xs, "avg", dtype, offsets=offsets)
+        for r in range(n):
+            assert_same_bits(got[r], want[r], dtype, f"offsets {offsets} rank {r}")
+    # reduce-scatter into compact buffers of every phase; all-gather from them
+    shards_want, _ = oracle.reduce_scatter(xs, "avg", dtype)
+    bounds = [oracle.chunk_range(length, n, c) for c in range(n)]
+    for off in range(per_vec):
+        sends = [Padded(length, dtype) for _ in range(n)]
+        for s, x in zip(sends, xs):
+            s.fill(x)
+        outs = [Padded(e - b, dtype, off + c) for c, (b, e) in enumerate(bounds)]
+        ra.ra_reduce_scatter([s.view for s in sends], [o.view for o in outs], "avg")
+        recvs = [Padded(length, dtype, off) for _ in range(n)]
+        ra.ra_allgather([o.view for o in outs], [r.view for r in recvs])
+        torch.cuda.synchronize()
+        for c in range(n):
+            assert outs[c].canaries_intact() and recvs[c].canaries_intact()
+            assert_same_bits(to_host(outs[c].view, dtype), shards_want[c], dtype, f"RS off {off}")
+            assert_same_bits(to_host(recvs[c].view, dtype), want[c], dtype, f"AG off {off}")
+
+
+def test_fewer_elements_than_ranks(ra):
+    # empty chunks: L < N (infra-guide 3.4 example: 3 elements over 4 ranks)
+    for n, length in ((4, 3), (16, 5), (64, 63), (7, 1)):
+        for dtype in ("f32", "i32"):
+            xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, "sum"), seed_base=n)
+            check_all(ra, xs, "sum", dtype, f"n={n} L={length}")
+
+
+def test_max_ranks(ra):
+    n, length = 64, 64 * 129 + 7
+    xs = inputs.rank_buffers(n, length, "f32", ("normal", 1.0), seed_base=2)
+    check_all(ra, xs, "sum", "f32", "64 ranks")
+
+
+def test_errors_enqueue_nothing(ra):
+    x = torch.ones(100, device="cuda")
+    y = torch.zeros(100, device="cuda")
+    with pytest.raises(ra.RaError):
+        ra.ra_allreduce([x, x], [y, y], "sum")  # two ranks writing one buffer
+    torch.cuda.synchronize()
+    assert (y == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads in the benchmark's launch configuration: sampled outputs
+# ---------------------------------------------------------------------------
+def _host_ram_gb():
+    with open("/proc/meminfo") as f:
+        for ln in f:
+            if ln.startswith("MemAvailable"):
+                return int(ln.split()[1]) / 2**20
+    return 0.0
+
+
+def sample_indices(length, n, k=1 << 17, seed=0):
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(0, length, size=k, dtype=np.int64), np.arange(min(64, length)),
+           np.arange(max(0, length - 64), length)]
+    for c in range(1, n):
+        b = c * length // n
+        idx.append(np.arange(max(0, b - 4), min(length, b + 5)))
+    return np.unique(np.concatenate(idx)).astype(np.int64)
+
+
+def check_full_size(ra, n, length, dtype, op, dist):
+    need_gb = 2.5 * n * length * ELEM_SIZE[dtype] / 2**30
+    if _host_ram_gb() < need_gb + 4:
+        pytest.skip(f"host RAM below {need_gb + 4:.0f} GB")
+    xs = inputs.rank_buffers(n, length, dtype, dist)
+    sends = [to_device(x, dtype) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    ra.ra_allreduce(sends, recvs, op)
+    torch.cuda.synchronize()
+    for r in range(1, n):
+        assert torch.equal(recvs[r].view(torch.uint8), recvs[0].view(torch.uint8)), f"rank {r} differs"
+    idx = sample_indices(length, n)
+    got = to_host(recvs[0][torch.from_numpy(idx).cuda()], dtype)
+    want = oracle.fold_at(xs, op, dtype, idx)
+    assert_same_bits(got, want, dtype, f"sampled n={n} L={length}")
+    del sends, recvs
+    torch.cuda.empty_cache()
+
+
+def test_full_size_n8_f32_avg_64m(ra):
+    n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_f32_avg_64m"]
+    check_full_size(ra, n, length, dtype, op, dist)
+
+
+def test_full_size_n8_bf16_avg_gpt2m(ra):
+    n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_bf16_avg_gpt2m"]
+    check_full_size(ra, n, length, dtype, op, dist)
+
+
+@pytest.mark.parametrize("n,length", [(n, 1 << p) for n in (8, 16) for p in (8, 10, 12, 14, 16, 18, 20)])
+def test_size_sweep_small(ra, n, length):
+    xs = inputs.rank_buffers(n, length, "f32", ("uniform", -1.0, 1.0))
+    check_all(ra, xs, "sum", "f32", f"sweep n={n} L={length}")
+
+
+@pytest.mark.parametrize("n,length", [(8, 1 << 24), (16, 1 << 26), (16, 1 << 28)])
+def test_size_sweep_large(ra, n, length):
+    check_full_size(ra, n, length, "f32", "sum", ("uniform", -1.0, 1.0))
