@@ -113,6 +113,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(used), "in_timed_region": len(inside)}
 
 
+def max_over_ranks(ms: float, world: int, device: str) -> float:
+    """The slowest rank's time: the job is done when every replica is done."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job algorithm bandwidth: every replica reduces bytes_per_rank per step."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / GB
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ring_all_reduce_02_gb300", "csrc")
@@ -265,18 +282,13 @@ def run_ours(args):
     t_wall1 = time.time()
     launches = args.steps  # one fused kernel per call
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms, per launch
-    total_ms = starts[0].elapsed_time(ends[-1])
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=f"cuda:{dev}")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), world, f"cuda:{dev}")
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
 
     ms_per_step = total_ms / args.steps
-    value = world * s_bytes / (ms_per_step * 1e-3) / GB
+    value = job_value(s_bytes, world, ms_per_step)
     avg_launch_ms = sum(per) / len(per)
     peak, peak_kind = measured_peaks()
     achieved = 2 * n * s_bytes / (avg_launch_ms * 1e-3) / GB
@@ -303,13 +315,8 @@ def run_ours(args):
             p.copy_(r, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device=f"cuda:{dev}")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * s_bytes / (e2e_ms * 1e-3) / GB
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, f"cuda:{dev}")
+    e2e_value = job_value(s_bytes, world, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -107,6 +107,21 @@ ra_status_t ra_allgather(const void* const* sendbufs, void* const* recvbufs, siz
                          ra_dtype_t dtype, ra_op_t op, int nranks, void* stream);
 
 /*
+ * The literal ring schedule, one kernel launch per ring step (tirogla.com
+ * "Ring all-reduce", "How it works"): reduce-scatter step s = 0..N-2 has rank
+ * r combine chunk (r-s-1) mod N arriving from rank r-1 with its own copy;
+ * all-gather step s has rank r copy chunk (r-s) mod N from rank r-1. Every
+ * message is a read of rank r-1's buffer in HBM. Same arguments, rounding,
+ * in-place rule and final result (bit for bit) as ra_allreduce; it moves
+ * about 5(N-1)*S bytes instead of 2N*S, which is what the fused kernel saves.
+ * nsteps: run only the first nsteps of the 2(N-1) steps (negative = all);
+ * after a partial run each rank's buffer holds the schedule's state for the
+ * chunks the steps have touched and is undefined elsewhere.
+ */
+ra_status_t ra_allreduce_ringsteps(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                   ra_dtype_t dtype, ra_op_t op, int nranks, int nsteps, void* stream);
+
+/*
  * Chunk bounds (tirogla.com "Ring all-reduce", section "Code"):
  * *begin = c*count/nranks, *end = (c+1)*count/nranks, floor division, exact
  * for every count <= RA_MAX_COUNT. Host only; touches no GPU.

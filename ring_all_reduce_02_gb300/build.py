@@ -48,15 +48,17 @@ def _deps_newer(target: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _deps_newer(LIB):
-        return LIB
+def build(force: bool = False, verbose: bool = False, defines=(), lib_path: str = LIB) -> str:
+    """Compile and link; ``defines`` ("NAME=VALUE") override the kernels' build-time tunables."""
+    if not force and not _deps_newer(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if verbose else []
+    out_dir = OUT_DIR if lib_path == LIB else lib_path + ".objs"
+    os.makedirs(out_dir, exist_ok=True)
+    extra = (["-Xptxas", "-v"] if verbose else []) + [f"-D{d}" for d in defines]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,13 +70,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -106,18 +106,14 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
   a->head = (int)(((ra::kVecBytes - phase) % ra::kVecBytes) / (unsigned)es);
   a->vec_ok = same ? 1 : 0;
   a->inv_n = 1.0f / (float)nranks;
+  a->step = 0;
   return RA_SUCCESS;
 }
 
-ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, size_t count,
-                ra_dtype_t dtype, ra_op_t op, int nranks, void* stream) {
-  ra::Args a;
-  if (kind == ra::KIND_ALLGATHER) op = RA_SUM;  // no reduction; any valid op is accepted
-  const ra_status_t st = prepare(kind, sendbufs, recvbufs, count, dtype, op, nranks, &a);
-  if (st != RA_SUCCESS || count == 0) return st;
-
-  // Grid: blockIdx.y = chunk; blockIdx.x = CTAs sharing that chunk, enough to
-  // cover the chunk's vectors but no more than one resident wave in total.
+// Grid: blockIdx.y = chunk (or rank, for the ring steps); blockIdx.x = CTAs
+// sharing it, enough to cover its vectors (per_thread of them per thread) but
+// no more than one resident wave in total.
+ra_status_t grid_for(const ra::Args& a, int dtype, int per_thread, dim3* grid) {
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -127,15 +123,21 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   }
   const int es = elem_size(dtype);
   const uint64_t v = (uint64_t)(ra::kVecBytes / es);
-  const uint64_t per_chunk = (count + (uint64_t)nranks - 1) / (uint64_t)nranks;
+  const uint64_t n = (uint64_t)a.nranks;
+  const uint64_t per_chunk = (a.count + n - 1) / n;
   const uint64_t work = a.vec_ok ? (per_chunk / v + 1) : per_chunk;  // vectors, or elements
-  const uint64_t per_cta = a.vec_ok ? (uint64_t)ra::kThreads * ra::kUnroll : (uint64_t)ra::kThreads;
+  const uint64_t per_cta = a.vec_ok ? (uint64_t)ra::kThreads * per_thread : (uint64_t)ra::kThreads;
   uint64_t gx = (work + per_cta - 1) / per_cta;
-  const uint64_t cap = (uint64_t)sms * ra::kMinBlocks / (uint64_t)nranks;
+  const uint64_t cap = (uint64_t)sms * ra::kMinBlocks / n;
   if (gx > cap) gx = cap;
   if (gx < 1) gx = 1;
-  const dim3 grid((unsigned)gx, (unsigned)nranks);
+  *grid = dim3((unsigned)gx, (unsigned)a.nranks);
+  return RA_SUCCESS;
+}
+
+ra_status_t launch(int kind, int dtype, int op, const ra::Args& a, dim3 grid, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
   switch (dtype) {
     case RA_FLOAT32: err = ra::launch_f32(kind, op, a, grid, s); break;
     case RA_FLOAT16: err = ra::launch_f16(kind, op, a, grid, s); break;
@@ -146,6 +148,41 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   if (err != cudaSuccess) {
     g_last_cuda_error = (int)err;
     return RA_ERR_CUDA;
+  }
+  return RA_SUCCESS;
+}
+
+ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, size_t count,
+                ra_dtype_t dtype, ra_op_t op, int nranks, void* stream) {
+  ra::Args a;
+  if (kind == ra::KIND_ALLGATHER) op = RA_SUM;  // no reduction; any valid op is accepted
+  ra_status_t st = prepare(kind, sendbufs, recvbufs, count, dtype, op, nranks, &a);
+  if (st != RA_SUCCESS || count == 0) return st;
+  dim3 grid;
+  st = grid_for(a, dtype, ra::kUnroll, &grid);
+  if (st != RA_SUCCESS) return st;
+  return launch(kind, dtype, op, a, grid, stream);
+}
+
+ra_status_t run_ringsteps(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                          ra_dtype_t dtype, ra_op_t op, int nranks, int nsteps, void* stream) {
+  ra::Args a;
+  ra_status_t st = prepare(ra::KIND_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, nranks, &a);
+  if (st != RA_SUCCESS || count == 0) return st;
+  const int total = 2 * (nranks - 1);
+  if (nsteps < 0 || nsteps > total) nsteps = total;
+  dim3 grid;
+  if (nranks == 1) {  // no ring steps: the result is the (avg-scaled) copy
+    st = grid_for(a, dtype, ra::kUnroll, &grid);
+    return st != RA_SUCCESS ? st : launch(ra::KIND_ALLREDUCE, dtype, op, a, grid, stream);
+  }
+  st = grid_for(a, dtype, 1, &grid);
+  if (st != RA_SUCCESS) return st;
+  for (int k = 0; k < nsteps; ++k) {
+    const bool rs = k < nranks - 1;
+    a.step = rs ? k : k - (nranks - 1);
+    st = launch(rs ? ra::KIND_RING_RS_STEP : ra::KIND_RING_AG_STEP, dtype, op, a, grid, stream);
+    if (st != RA_SUCCESS) return st;
   }
   return RA_SUCCESS;
 }
@@ -167,6 +204,11 @@ ra_status_t ra_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
 ra_status_t ra_allgather(const void* const* sendbufs, void* const* recvbufs, size_t count,
                          ra_dtype_t dtype, ra_op_t op, int nranks, void* stream) {
   return run(ra::KIND_ALLGATHER, sendbufs, recvbufs, count, dtype, op, nranks, stream);
+}
+
+ra_status_t ra_allreduce_ringsteps(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                   ra_dtype_t dtype, ra_op_t op, int nranks, int nsteps, void* stream) {
+  return run_ringsteps(sendbufs, recvbufs, count, dtype, op, nranks, nsteps, stream);
 }
 
 ra_status_t ra_chunk_range(size_t count, int nranks, int c, size_t* begin, size_t* end) {

@@ -31,12 +31,32 @@
 
 namespace ra {
 
-constexpr int kThreads = 256;   // threads per CTA
-constexpr int kMinBlocks = 2;   // resident CTAs per SM the register budget is set for
-constexpr int kUnroll = 2;      // 16-byte vectors per thread per trip
-constexpr int kBatch = 8;       // ranks whose loads are in flight together
+// Launch shape (build-time overridable for tuning sweeps; these defaults are the
+// measured choice on GB300).
+#ifndef RA_THREADS
+#define RA_THREADS 256
+#endif
+#ifndef RA_MIN_BLOCKS
+#define RA_MIN_BLOCKS 2
+#endif
+#ifndef RA_UNROLL
+#define RA_UNROLL 2
+#endif
+#ifndef RA_BATCH
+#define RA_BATCH 8
+#endif
+constexpr int kThreads = RA_THREADS;       // threads per CTA
+constexpr int kMinBlocks = RA_MIN_BLOCKS;  // resident CTAs per SM the register budget is set for
+constexpr int kUnroll = RA_UNROLL;         // 16-byte vectors per thread per trip
+constexpr int kBatch = RA_BATCH;           // ranks whose loads are in flight together
 
-enum Kind { KIND_ALLREDUCE = 0, KIND_REDUCE_SCATTER = 1, KIND_ALLGATHER = 2 };
+enum Kind {
+  KIND_ALLREDUCE = 0,       // fused: one launch per call
+  KIND_REDUCE_SCATTER = 1,  // fused
+  KIND_ALLGATHER = 2,       // fused
+  KIND_RING_RS_STEP = 3,    // one reduce-scatter step of the literal schedule, all ranks
+  KIND_RING_AG_STEP = 4,    // one all-gather step of the literal schedule, all ranks
+};
 
 // Kernel parameters, passed by value (no device allocation, no state).
 struct Args {
@@ -48,6 +68,7 @@ struct Args {
   int head;    // first element index on the common 16-byte grid, in [0, V)
   int vec_ok;  // the N-way side (AR/RS: sources and AR destinations; AG: destinations) shares one phase
   float inv_n; // 1.0f / nranks, rounded in fp32
+  int step;    // ring step of a KIND_RING_* launch
 };
 
 // ---------------------------------------------------------------------------
@@ -247,6 +268,67 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) ag_copy_kernel(const __g
 }
 
 // ---------------------------------------------------------------------------
+// The literal schedule, one launch per ring step (for checking and measuring
+// the fused kernels against it). blockIdx.y = rank r.
+//
+// reduce-scatter step s: rank r receives chunk C = (r - s - 1) mod N from rank
+// r-1 and combines it with its own copy: dst[r][C] = hop(in, src[r][C]), where
+// `in` is rank r-1's partial of C from step s-1 (dst[r-1][C]) or, at s = 0,
+// its input (src[r-1][C]). Each chunk of rank r is touched once in this phase,
+// so its own operand is still its input, read from src[r]; in place
+// (dst == src) this is the same memory. At s = N-2 rank r finishes chunk
+// (r+1) mod N and applies the avg epilogue to it.
+// all-gather step s: dst[r][C] = dst[r-1][C] with C = (r - s) mod N.
+// ---------------------------------------------------------------------------
+template <int DT, int OP>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) ring_rs_step_kernel(const __grid_constant__ Args a) {
+  constexpr int V = Elem<DT>::kPerVec;
+  constexpr int ES = Elem<DT>::kSize;
+  const int n = a.nranks, r = blockIdx.y, s = a.step;
+  const int prev = r == 0 ? n - 1 : r - 1;
+  const int cc = ((r - s - 1) % n + n) % n;
+  const void* in = s == 0 ? a.src[prev] : a.dst[prev];
+  const void* own = a.src[r];
+  void* out = a.dst[r];
+  const bool finish = (OP == OP_AVG) && (s == n - 2);
+  const uint64_t b0 = chunk_begin(cc, n, a.count), b1 = chunk_begin(cc + 1, n, a.count);
+  uint64_t vb = b0, ve = b0;
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  const uint64_t nv = (ve - vb) / V;
+  for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < nv; j += (uint64_t)gridDim.x * kThreads) {
+    const uint64_t off = (vb + j * V) * ES;
+    uint4 v = vec_hop<DT, OP>(ld_vec(static_cast<const char*>(in) + off), ld_vec(static_cast<const char*>(own) + off));
+    if (finish) v = vec_avg<DT>(v, a.inv_n, n);
+    st_vec(static_cast<char*>(out) + off, v);
+  }
+  for_each_edge_elem(b0, vb, ve, b1, [&](uint64_t i) {
+    uint32_t v = elem_hop<DT, OP>(ld_elem<DT>(in, i), ld_elem<DT>(own, i));
+    if (finish) v = elem_avg<DT>(v, a.inv_n, n);
+    st_elem<DT>(out, i, v);
+  });
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) ring_ag_step_kernel(const __grid_constant__ Args a) {
+  constexpr int V = Elem<DT>::kPerVec;
+  constexpr int ES = Elem<DT>::kSize;
+  const int n = a.nranks, r = blockIdx.y, s = a.step;
+  const int prev = r == 0 ? n - 1 : r - 1;
+  const int cc = ((r - s) % n + n) % n;
+  const void* in = a.dst[prev];
+  void* out = a.dst[r];
+  const uint64_t b0 = chunk_begin(cc, n, a.count), b1 = chunk_begin(cc + 1, n, a.count);
+  uint64_t vb = b0, ve = b0;
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  const uint64_t nv = (ve - vb) / V;
+  for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < nv; j += (uint64_t)gridDim.x * kThreads) {
+    const uint64_t off = (vb + j * V) * ES;
+    st_vec(static_cast<char*>(out) + off, ld_vec(static_cast<const char*>(in) + off));
+  }
+  for_each_edge_elem(b0, vb, ve, b1, [&](uint64_t i) { st_elem<DT>(out, i, ld_elem<DT>(in, i)); });
+}
+
+// ---------------------------------------------------------------------------
 // host-side launch for one dtype (instantiated once per dtype translation unit)
 // ---------------------------------------------------------------------------
 template <int DT>
@@ -256,10 +338,15 @@ cudaError_t launch_dtype(int kind, int op, const Args& a, dim3 grid, cudaStream_
     ag_copy_kernel<DT><<<grid, block, 0, s>>>(a);
     return cudaGetLastError();
   }
-#define RA_LAUNCH_OP(OPV)                                                   \
-  case OPV:                                                                 \
-    if (kind == KIND_ALLREDUCE) ar_fused_kernel<DT, OPV><<<grid, block, 0, s>>>(a); \
-    else rs_fused_kernel<DT, OPV><<<grid, block, 0, s>>>(a);                \
+  if (kind == KIND_RING_AG_STEP) {
+    ring_ag_step_kernel<DT><<<grid, block, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+#define RA_LAUNCH_OP(OPV)                                                            \
+  case OPV:                                                                          \
+    if (kind == KIND_ALLREDUCE) ar_fused_kernel<DT, OPV><<<grid, block, 0, s>>>(a);  \
+    else if (kind == KIND_REDUCE_SCATTER) rs_fused_kernel<DT, OPV><<<grid, block, 0, s>>>(a); \
+    else ring_rs_step_kernel<DT, OPV><<<grid, block, 0, s>>>(a);                     \
     break;
   switch (op) {
     RA_LAUNCH_OP(OP_SUM)

@@ -173,11 +173,27 @@ __device__ __forceinline__ uint32_t vec_lane(const uint4& v, int l) {
 
 // ---- global memory ----------------------------------------------------------
 // Streaming (evict-first) 16-byte loads and stores: every byte is touched once.
+// RA_LD_MODE / RA_ST_MODE select other cache hints for tuning sweeps
+// (0 = evict-first streaming, 1 = default caching).
+#ifndef RA_LD_MODE
+#define RA_LD_MODE 0
+#endif
+#ifndef RA_ST_MODE
+#define RA_ST_MODE 0
+#endif
 __device__ __forceinline__ uint4 ld_vec(const void* p) {
+#if RA_LD_MODE == 0
   return __ldcs(reinterpret_cast<const uint4*>(p));
+#else
+  return *reinterpret_cast<const uint4*>(p);
+#endif
 }
 __device__ __forceinline__ void st_vec(void* p, uint4 v) {
+#if RA_ST_MODE == 0
   __stcs(reinterpret_cast<uint4*>(p), v);
+#else
+  *reinterpret_cast<uint4*>(p) = v;
+#endif
 }
 template <int DT>
 __device__ __forceinline__ uint32_t ld_elem(const void* base, uint64_t i) {

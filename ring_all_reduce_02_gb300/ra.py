@@ -22,8 +22,8 @@ OP_CODES = {"sum": 0, "avg": 1, "min": 2, "max": 3, "prod": 4}
 RA_MAX_RANKS = 64
 
 # every symbol include/ra.h declares
-EXPORTS = ("ra_allreduce", "ra_reduce_scatter", "ra_allgather", "ra_chunk_range", "ra_plan_chunk",
-           "ra_status_string", "ra_last_cuda_error")
+EXPORTS = ("ra_allreduce", "ra_reduce_scatter", "ra_allgather", "ra_allreduce_ringsteps", "ra_chunk_range",
+           "ra_plan_chunk", "ra_status_string", "ra_last_cuda_error")
 
 
 class RaError(RuntimeError):
@@ -54,6 +54,8 @@ def lib() -> ctypes.CDLL:
                 f = getattr(L, name)
                 f.argtypes = [PP, PP, SZ, I, I, I, VP]
                 f.restype = I
+            L.ra_allreduce_ringsteps.argtypes = [PP, PP, SZ, I, I, I, I, VP]
+            L.ra_allreduce_ringsteps.restype = I
             L.ra_chunk_range.argtypes = [SZ, I, I, PSZ, PSZ]
             L.ra_chunk_range.restype = I
             L.ra_plan_chunk.argtypes = [SZ, I, I, I, I, PSZ, PSZ, PSZ, PSZ]
@@ -114,6 +116,20 @@ def ra_allreduce(sendbufs, recvbufs, op: str = "sum", stream=None) -> None:
               dtype_code(sendbufs[0]), OP_CODES[op], len(sendbufs), _stream_ptr(stream))
     if st:
         raise RaError(st, "ra_allreduce")
+
+
+def ra_allreduce_ringsteps(sendbufs, recvbufs, op: str = "sum", nsteps: int = -1, stream=None) -> None:
+    """The literal ring schedule, one launch per step (first ``nsteps`` of 2(N-1); -1 = all)."""
+    _check(list(sendbufs) + list(recvbufs), "ra_allreduce_ringsteps")
+    count = sendbufs[0].numel()
+    if any(t.numel() != count for t in list(sendbufs) + list(recvbufs)) or len(recvbufs) != len(sendbufs):
+        raise ValueError("ra_allreduce_ringsteps: N send and N recv buffers of one length")
+    st = lib().ra_allreduce_ringsteps(ptr_array([t.data_ptr() for t in sendbufs]),
+                                      ptr_array([t.data_ptr() for t in recvbufs]), count,
+                                      dtype_code(sendbufs[0]), OP_CODES[op], len(sendbufs), nsteps,
+                                      ctypes.c_void_p(_stream_ptr(stream) or None))
+    if st:
+        raise RaError(st, "ra_allreduce_ringsteps")
 
 
 def ra_reduce_scatter(sendbufs, recvbufs, op: str = "sum", stream=None) -> None:

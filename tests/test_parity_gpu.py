@@ -382,3 +382,41 @@ def test_size_sweep_small(ra, n, length):
 @pytest.mark.parametrize("n,length", [(8, 1 << 24), (16, 1 << 26), (16, 1 << 28)])
 def test_size_sweep_large(ra, n, length):
     check_full_size(ra, n, length, "f32", "sum", ("uniform", -1.0, 1.0))
+
+
+# ---------------------------------------------------------------------------
+# the literal schedule (one launch per ring step) against the oracle's steps
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("bf16", "avg"), ("f16", "prod"), ("i32", "max"),
+                                      ("f32", "avg"), ("bf16", "min")])
+def test_ringsteps_final_result(ra, dtype, op):
+    for n, length in ((1, 100), (2, 1001), (3, 1000), (4, 4096), (5, 1003), (8, 65536 + 3), (16, 999)):
+        xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=n)
+        want, _, _ = oracle.allreduce(xs, op, dtype)
+        fused = run_allreduce(ra, xs, op, dtype)
+        for inplace in (False, True):
+            sends = [to_device(x, dtype) for x in xs]
+            recvs = sends if inplace else [torch.empty_like(s) for s in sends]
+            ra.ra_allreduce_ringsteps(sends, recvs, op)
+            torch.cuda.synchronize()
+            for r in range(n):
+                got = to_host(recvs[r], dtype)
+                assert_same_bits(got, want[r], dtype, f"n={n} L={length} rank {r} inplace={inplace}")
+                assert got.tobytes() == fused[r].tobytes()
+
+
+def test_ringsteps_intermediate_states(ra):
+    # after k steps, every chunk a step has written holds the oracle's state at step k-1
+    n, length, dtype, op = 5, 1003, "i32", "sum"
+    xs = [np.full(length, 1 << r, dtype=np.int32) for r in range(n)]  # tags: partial = set of ranks
+    _, _, snaps = oracle.allreduce(xs, op, dtype, snapshots=True)
+    for k in range(1, 2 * (n - 1) + 1):
+        sends = [to_device(x, dtype) for x in xs]
+        recvs = [torch.zeros_like(s) for s in sends]
+        ra.ra_allreduce_ringsteps(sends, recvs, op, nsteps=k)
+        torch.cuda.synchronize()
+        s = k - 1
+        for r in range(n):
+            c = (r - s - 1) % n if s < n - 1 else (r - (s - (n - 1))) % n
+            b, e = oracle.chunk_range(length, n, c)
+            assert (to_host(recvs[r], dtype)[b:e] == snaps[s, r, b:e]).all(), (k, r, c)
