@@ -66,6 +66,8 @@ def _load():
             lib.ra_oracle_reduce_scatter.argtypes = [PP, PP, U64, I, I, I, I, P]
             lib.ra_oracle_allgather.argtypes = [PP, PP, U64, I, I, I, P, P]
             lib.ra_oracle_fold_at.argtypes = [PP, U64, I, I, I, P, U64, P]
+            lib.ra_oracle_allreduce_ex.argtypes = [PP, PP, U64, I, I, I, I, I, I, P]
+            lib.ra_oracle_allreduce_ex.restype = ctypes.c_int
             lib.ra_oracle_hop.argtypes = [I, I, P, P, P, U64]
             lib.ra_oracle_round.argtypes = [I, P, P, U64]
             lib.ra_oracle_widen.argtypes = [I, P, P, U64]
@@ -119,6 +121,26 @@ def allreduce(xs, op: str, dtype: str, timeout_ms: int = 10000, snapshots: bool 
     if st:
         raise OracleError(st, "allreduce")
     return outs, sent[:n], snaps
+
+
+ORDERS = {"ring": 0, "tree": 1, "rabenseifner": 2}
+ACCUMS = {"dtype": 0, "fp32": 1}
+
+
+def allreduce_ex(xs, op: str, dtype: str, order: str = "ring", accum: str = "dtype", timeout_ms: int = 10000):
+    """All-reduce by another algorithm or accumulation: order ring | tree (double binary tree) |
+    rabenseifner (power-of-two N); accum dtype | fp32 (ring only). Returns (outs, bytes_sent)."""
+    lib = _load()
+    n = len(xs)
+    length = xs[0].shape[0] if n else 0
+    _check_inputs(xs, dtype, length)
+    outs = [np.empty_like(x) for x in xs]
+    sent = np.zeros(max(n, 1), dtype=np.uint64)
+    st = lib.ra_oracle_allreduce_ex(_ptrs(xs), _ptrs(outs), length, DTYPES[dtype], OPS[op], n, ORDERS[order],
+                                    ACCUMS[accum], timeout_ms, sent.ctypes.data)
+    if st:
+        raise OracleError(st, "allreduce_ex")
+    return outs, sent[:n]
 
 
 def reduce_scatter(xs, op: str, dtype: str, timeout_ms: int = 10000):

@@ -384,6 +384,140 @@ struct Ring {
   }
 };
 
+// ---- a full mesh of channels, for the algorithms that talk to partners ----
+struct Mesh {
+  int n;
+  std::vector<Channel> chan;  // chan[src * n + dst]
+  int timeout_ms;
+  uint64_t* bytes_sent;
+  std::vector<int> status;
+  Mesh(int n_, int timeout, uint64_t* bytes)
+      : n(n_), chan((size_t)n_ * n_), timeout_ms(timeout), bytes_sent(bytes), status(n_, ORACLE_OK) {}
+  void send(int src, int dst, const uint8_t* p, size_t nb) {
+    chan[(size_t)src * n + dst].send(std::vector<uint8_t>(p, p + nb));
+    if (bytes_sent) bytes_sent[src] += nb;
+  }
+  bool recv(int src, int dst, std::vector<uint8_t>& in, size_t want) {
+    if (!chan[(size_t)src * n + dst].recv(in, timeout_ms)) {
+      status[dst] = ORACLE_TIMEOUT;
+      return false;
+    }
+    if (in.size() != want) {
+      status[dst] = ORACLE_PROTOCOL;
+      return false;
+    }
+    return true;
+  }
+  int result() const {
+    for (int s : status)
+      if (s != ORACLE_OK) return s;
+    return ORACLE_OK;
+  }
+};
+
+// Rabenseifner's all-reduce for a power-of-two number of ranks (tirogla.com
+// "Ring all-reduce", "How it works", cost model: recursive-halving
+// reduce-scatter followed by recursive-doubling all-gather). Halving step with
+// distance d = N/2, N/4, ..., 1: rank r and its partner r XOR d split their
+// current range in two; the rank whose d bit is clear keeps the lower half.
+// Each sends the half it gives up and combines the half it keeps with the
+// partner's copy, the lower rank's value on the left. The owner of a range
+// finishes avg on it; doubling then returns the halves in reverse order.
+void rabenseifner_rank(Mesh& M, int r, uint8_t* d, uint64_t len, int dt, int op, size_t es) {
+  const int n = M.n;
+  uint64_t lo = 0, hi = len;
+  std::vector<uint64_t> los, his;
+  std::vector<uint8_t> in;
+  for (int dist = n / 2; dist >= 1; dist /= 2) {
+    const int p = r ^ dist;
+    const uint64_t mid = lo + (hi - lo) / 2;
+    const bool lower = (r & dist) == 0;
+    const uint64_t keep_lo = lower ? lo : mid, keep_hi = lower ? mid : hi;
+    const uint64_t give_lo = lower ? mid : lo, give_hi = lower ? hi : mid;
+    los.push_back(lo);
+    his.push_back(hi);
+    M.send(r, p, d + give_lo * es, (give_hi - give_lo) * es);
+    if (!M.recv(p, r, in, (keep_hi - keep_lo) * es)) return;
+    for (uint64_t k = 0; k < keep_hi - keep_lo; ++k) {
+      uint8_t* mine = d + (keep_lo + k) * es;
+      const uint8_t* theirs = &in[k * es];
+      if (lower) hop(dt, op, mine, theirs, mine);
+      else hop(dt, op, theirs, mine, mine);
+    }
+    lo = keep_lo;
+    hi = keep_hi;
+  }
+  if (op == AVG)
+    for (uint64_t k = lo; k < hi; ++k) avg_epilogue(dt, n, d + k * es);
+  for (int dist = 1, step = (int)los.size() - 1; dist < n; dist *= 2, --step) {
+    const int p = r ^ dist;
+    const uint64_t plo = los[step], phi = his[step];
+    const uint64_t mid = plo + (phi - plo) / 2;
+    const bool lower = (r & dist) == 0;
+    const uint64_t other_lo = lower ? mid : plo, other_hi = lower ? phi : mid;
+    M.send(r, p, d + lo * es, (hi - lo) * es);
+    if (!M.recv(p, r, in, (other_hi - other_lo) * es)) return;
+    if (!in.empty()) std::memcpy(d + other_lo * es, in.data(), in.size());
+    lo = plo;
+    hi = phi;
+  }
+}
+
+// A binary tree laid over a sequence of ranks in order: the middle position
+// is the root, the two halves its subtrees. parent[] / left[] / right[] by rank.
+struct InorderTree {
+  std::vector<int> parent, left, right;
+  int root = -1;
+  InorderTree(const std::vector<int>& seq) : parent(seq.size(), -1), left(seq.size(), -1), right(seq.size(), -1) {
+    root = build(seq, 0, (int)seq.size() - 1, -1);
+  }
+  int build(const std::vector<int>& seq, int lo, int hi, int par) {
+    if (lo > hi) return -1;
+    const int m = (lo + hi) / 2, v = seq[m];
+    parent[v] = par;
+    left[v] = build(seq, lo, m - 1, v);
+    right[v] = build(seq, m + 1, hi, v);
+    return v;
+  }
+};
+
+// Double binary tree (tirogla.com "Ring all-reduce", cost model; NCCL's tree
+// since 2.4): two binary trees, each reducing half of the buffer up to its
+// root and broadcasting the result back down. Tree A is the in-order tree over
+// ranks 0..N-1 and reduces chunks [0, N/2); tree B is the in-order tree over
+// ranks N-1..0 and reduces chunks [N/2, N). A node folds in order: its left
+// subtree's partial, its own value, its right subtree's partial.
+void tree_rank(Mesh& M, int r, uint8_t* d, uint64_t len, int dt, int op, size_t es) {
+  const int n = M.n;
+  std::vector<int> fwd(n), bwd(n);
+  for (int i = 0; i < n; ++i) fwd[i] = i, bwd[i] = n - 1 - i;
+  const uint64_t split = chunk_begin(n / 2, n, len);
+  std::vector<uint8_t> in;
+  for (int t = 0; t < 2; ++t) {
+    const InorderTree T(t == 0 ? fwd : bwd);
+    const uint64_t lo = t == 0 ? 0 : split, hi = t == 0 ? split : len;
+    const size_t nb = (hi - lo) * es;
+    uint8_t* mine = d + lo * es;
+    if (T.left[r] >= 0) {  // partial of the left subtree, then own value on the right
+      if (!M.recv(T.left[r], r, in, nb)) return;
+      for (uint64_t k = 0; k < hi - lo; ++k) hop(dt, op, &in[k * es], mine + k * es, mine + k * es);
+    }
+    if (T.right[r] >= 0) {  // then the right subtree's partial on the right
+      if (!M.recv(T.right[r], r, in, nb)) return;
+      for (uint64_t k = 0; k < hi - lo; ++k) hop(dt, op, mine + k * es, &in[k * es], mine + k * es);
+    }
+    if (T.parent[r] >= 0) {
+      M.send(r, T.parent[r], mine, nb);
+      if (!M.recv(T.parent[r], r, in, nb)) return;  // the result, broadcast down
+      if (nb) std::memcpy(mine, in.data(), nb);
+    } else if (op == AVG) {
+      for (uint64_t k = 0; k < hi - lo; ++k) avg_epilogue(dt, n, mine + k * es);
+    }
+    if (T.left[r] >= 0) M.send(r, T.left[r], mine, nb);
+    if (T.right[r] >= 0) M.send(r, T.right[r], mine, nb);
+  }
+}
+
 int check_args(uint64_t len, int dt, int op, int n) {
   if (n < 1 || n > kMaxRanks) return ORACLE_INVALID;
   if (elem_size(dt) == 0) return ORACLE_INVALID;
@@ -515,6 +649,84 @@ int ra_oracle_allgather(const void* const* send, void* const* recv, uint64_t len
   }
   for (auto& t : threads) t.join();
   return R.result();
+}
+
+// All-reduce with a choice of algorithm (order) and accumulation precision.
+// order 0 = ring (as ra_oracle_allreduce), 1 = double binary tree,
+// 2 = Rabenseifner (power-of-two n only). accum 0 = every hop rounded to the
+// dtype; accum 1 = fp16/bf16 partials travel as fp32 messages and the owner
+// rounds once, after the avg multiply (tirogla.com "Ring all-reduce",
+// "Implementation notes": bf16 with fp32 accumulation at large N); for fp32 and
+// int32 buffers accum 1 is the same as accum 0. accum 1 is defined for the
+// ring only.
+int ra_oracle_allreduce_ex(const void* const* send, void* const* recv, uint64_t len, int dtype, int op,
+                           int n, int order, int accum, int timeout_ms, uint64_t* bytes_sent) {
+  int st = check_args(len, dtype, op, n);
+  if (st != ORACLE_OK) return st;
+  if (order < 0 || order > 2 || accum < 0 || accum > 1) return ORACLE_INVALID;
+  if (order == 2 && (n & (n - 1))) return ORACLE_UNSUPPORTED;
+  if (accum == 1 && order != 0) return ORACLE_UNSUPPORTED;
+  const bool narrow = dtype == F16 || dtype == BF16;
+  if (order == 0 && (accum == 0 || !narrow))
+    return ra_oracle_allreduce(send, recv, len, dtype, op, n, timeout_ms, bytes_sent, nullptr, -1, -1);
+  const size_t es = elem_size(dtype);
+  if (bytes_sent) std::memset(bytes_sent, 0, sizeof(uint64_t) * n);
+  if (order == 0) {
+    // ring with fp32 messages: run the reduce-scatter phase on widened copies,
+    // round the owned chunk once, then the all-gather phase in the dtype
+    const Narrow& f = dtype == F16 ? kF16 : kBF16;
+    std::vector<std::vector<float>> w(n, std::vector<float>(len));
+    for (int r = 0; r < n; ++r)
+      for (uint64_t k = 0; k < len; ++k) w[r][k] = narrow_to_f32(((const uint16_t*)send[r])[k], f);
+    if (n == 1) {
+      for (uint64_t k = 0; k < len; ++k) {
+        float v = w[0][k];
+        if (op == AVG) v = v * (1.0f / (float)n);
+        ((uint16_t*)recv[0])[k] = f32_to_narrow(v, f);
+      }
+      return ORACLE_OK;
+    }
+    Ring rs(n), ag(n);
+    rs.len = ag.len = len;
+    rs.dt = F32;
+    ag.dt = dtype;
+    rs.op = ag.op = op;
+    rs.es = 4;
+    ag.es = es;
+    rs.timeout_ms = ag.timeout_ms = timeout_ms;
+    rs.bytes_sent = ag.bytes_sent = bytes_sent;
+    std::vector<std::thread> threads;
+    for (int r = 0; r < n; ++r) {
+      threads.emplace_back([&, r] {
+        if (!rs.reduce_scatter_phase(r, (uint8_t*)w[r].data())) return;
+        const int own = (r + 1) % n;
+        uint16_t* out = (uint16_t*)recv[r];
+        for (uint64_t k = chunk_begin(own, n, len); k < chunk_end(own, n, len); ++k)
+          out[k] = f32_to_narrow(w[r][k], f);
+        ag.all_gather_phase(r, (uint8_t*)recv[r], /*shift=*/1, /*step_base=*/0);
+      });
+    }
+    for (auto& t : threads) t.join();
+    const int a = rs.result();
+    return a != ORACLE_OK ? a : ag.result();
+  }
+  for (int r = 0; r < n; ++r)
+    if (recv[r] != send[r]) std::memcpy(recv[r], send[r], len * es);
+  if (n == 1) {
+    if (op == AVG)
+      for (uint64_t k = 0; k < len; ++k) avg_epilogue(dtype, 1, (uint8_t*)recv[0] + k * es);
+    return ORACLE_OK;
+  }
+  Mesh M(n, timeout_ms, bytes_sent);
+  std::vector<std::thread> threads;
+  for (int r = 0; r < n; ++r) {
+    threads.emplace_back([&, r] {
+      if (order == 1) tree_rank(M, r, (uint8_t*)recv[r], len, dtype, op, es);
+      else rabenseifner_rank(M, r, (uint8_t*)recv[r], len, dtype, op, es);
+    });
+  }
+  for (auto& t : threads) t.join();
+  return M.result();
 }
 
 // The plain definition at selected indices, with no message passing: element
