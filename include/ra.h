@@ -32,14 +32,20 @@
  *  - sendbufs / recvbufs are host arrays of `nranks` device pointers. The
  *    arrays are read during the call only; the device buffers belong to the
  *    caller and must stay alive until the work on `stream` has completed.
- *  - The library allocates nothing and keeps no state between calls; calls
- *    are reentrant. Work is enqueued on `stream` (a cudaStream_t; NULL = the
- *    legacy default stream) and the call returns without waiting.
+ *  - The library allocates no device memory and keeps no state between
+ *    calls; calls are reentrant. Work is enqueued on `stream` (a
+ *    cudaStream_t; NULL = the legacy default stream) and the call returns
+ *    without waiting.
  *  - Arguments are checked on the host before any launch; on any error
  *    nothing is enqueued. Every pointer must be aligned to the element size;
  *    a pointer to a zero-length buffer may be NULL. Any other alignment is
- *    accepted: the 16-byte vector path is used when the buffers share their
- *    address modulo 16, a per-element path otherwise.
+ *    accepted: the vector path is used when the buffers share their address
+ *    modulo ra_vector_bytes(), a per-element path otherwise.
+ *  - Buffers may be device memory or host memory the device can address
+ *    (pinned host memory under unified addressing, or any host memory on
+ *    systems whose GPU accesses system memory coherently): the kernels then
+ *    read and write host memory directly over the host link, which replaces
+ *    explicit copies for callers whose data lives on the host.
  *  - Buffers must not overlap, except in the exact in-place layout named for
  *    each call (each element is then read and written by the same thread).
  *    Send buffers may overlap each other (they are only read).
@@ -106,6 +112,77 @@ ra_status_t ra_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
 ra_status_t ra_allgather(const void* const* sendbufs, void* const* recvbufs, size_t count,
                          ra_dtype_t dtype, ra_op_t op, int nranks, void* stream);
 
+/* Reduction order (the algorithm whose association the result reproduces). */
+typedef enum {
+  RA_ORDER_RING = 0,         /* tirogla.com "Ring all-reduce", "How it works" (the default) */
+  RA_ORDER_TREE = 1,         /* double binary tree (same page, cost model): in-order trees over ranks
+                                0..N-1 (first N/2 chunks) and N-1..0 (the rest) */
+  RA_ORDER_RABENSEIFNER = 2  /* recursive halving / doubling, power-of-two nranks (same page) */
+} ra_order_t;
+
+/* Precision of the partials travelling between ranks. */
+typedef enum {
+  RA_ACCUM_DTYPE = 0, /* every hop rounded to the buffer dtype (the default) */
+  RA_ACCUM_FP32 = 1   /* fp16/bf16: partials kept in fp32, rounded once at the end (after the
+                         avg multiply); tirogla.com "Ring all-reduce", "Implementation notes".
+                         No effect on fp32 and int32 buffers. */
+} ra_accum_t;
+
+/* Options of the extended calls; NULL means all defaults. */
+typedef struct {
+  ra_order_t order; /* RA_ORDER_RING by default */
+  ra_accum_t accum; /* RA_ACCUM_DTYPE by default */
+  int max_sms;      /* 0: the launch may fill every SM; k > 0: at most k SMs' worth of CTAs, leaving the
+                       rest to work running beside the collective (arjunsriva.com "AllReduce, All the Way
+                       Down": communication kernels compete with compute for SMs) */
+} ra_options_t;
+
+/*
+ * All-reduce / reduce-scatter with options: ra_allreduce(...) is
+ * ra_allreduce_ex(..., NULL, stream). Same buffers, in-place rules and errors
+ * as the plain calls, plus RA_ERR_UNSUPPORTED for RA_ORDER_RABENSEIFNER with a
+ * nranks that is not a power of two and for RA_ACCUM_FP32 with an order other
+ * than the ring, and RA_ERR_INVALID_ARG for an unknown order/accum or a
+ * negative max_sms.
+ */
+ra_status_t ra_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, size_t count, ra_dtype_t dtype,
+                            ra_op_t op, int nranks, const ra_options_t* options, void* stream);
+ra_status_t ra_reduce_scatter_ex(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                 ra_dtype_t dtype, ra_op_t op, int nranks, const ra_options_t* options,
+                                 void* stream);
+
+/*
+ * Gradient buckets (bitfern.com "AllReduce Explained", "PyTorch DDP and
+ * Gradient Synchronization"; tirogla.com "Ring all-reduce", "Implementation
+ * notes": DDP's default bucket is 25 MB). Host only, touches no GPU.
+ * param_counts[nparams]: element counts of the parameters, laid out
+ * contiguously in this order in the flat gradient buffer. Parameters are
+ * visited in reverse (the order backward produces their gradients) and packed
+ * into buckets of at most bucket_bytes (a parameter larger than that gets its
+ * own bucket). Writes up to max_buckets contiguous element ranges
+ * [bucket_begin[b], bucket_begin[b] + bucket_count[b]) in the order they
+ * become ready, and the number of buckets to *nbuckets (also when max_buckets
+ * is too small, which returns RA_ERR_INVALID_ARG; NULL arrays with
+ * max_buckets 0 query the count).
+ */
+ra_status_t ra_bucket_plan(const size_t* param_counts, int nparams, size_t bucket_bytes, int elem_size,
+                           size_t* bucket_begin, size_t* bucket_count, int max_buckets, int* nbuckets);
+
+/*
+ * Bucketed all-reduce: bucket b (an element range of every rank's buffer,
+ * listed in ascending or descending order, disjoint) is all-reduced as an
+ * all-reduce of its own (its own chunk bounds), after `stream` waits for
+ * ready_events[b] (a cudaEvent_t the producer recorded when the bucket's
+ * gradients were complete; NULL entries or a NULL array wait for nothing).
+ * The waits and launches are enqueued on `stream` in bucket order, so buckets
+ * overlap with work on other streams as soon as they are ready. Buffers,
+ * in-place rule and options as ra_allreduce_ex.
+ */
+ra_status_t ra_allreduce_buckets(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                 ra_dtype_t dtype, ra_op_t op, int nranks, int nbuckets, const size_t* bucket_begin,
+                                 const size_t* bucket_count, void* const* ready_events,
+                                 const ra_options_t* options, void* stream);
+
 /*
  * The literal ring schedule, one kernel launch per ring step (tirogla.com
  * "Ring all-reduce", "How it works"): reduce-scatter step s = 0..N-2 has rank
@@ -144,6 +221,10 @@ const char* ra_status_string(ra_status_t status);
 
 /* The cudaError_t of the last RA_ERR_CUDA returned on the calling thread (0 if none). */
 int ra_last_cuda_error(void);
+
+/* Bytes per vector access of this build's kernels (16 or 32): the address
+ * phase (address mod this) the buffers must share for the vector path. */
+int ra_vector_bytes(void);
 
 #ifdef __cplusplus
 }

@@ -1,17 +1,24 @@
 // The C ABI of libra.so: argument checks, the alias rules, the chunk-schedule
-// planner (grid sizing and vector-path selection) and dispatch to the fused
-// kernels. Declarations and the contract of every entry point: include/ra.h.
+// planner (grid sizing, launch shape and vector-path selection, the reduction
+// programs of the other orders, gradient buckets) and dispatch to the kernels.
+// Declarations and the contract of every entry point: include/ra.h.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "../../include/ra.h"
 #include "ra_kernels.cuh"
+#include "ra_order.cuh"
 
 namespace ra {
 cudaError_t launch_f32(int kind, int op, const Args& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_f16(int kind, int op, const Args& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_bf16(int kind, int op, const Args& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_i32(int kind, int op, const Args& a, dim3 grid, cudaStream_t s);
+cudaError_t launch_ordered_f32(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
+cudaError_t launch_ordered_f16(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
+cudaError_t launch_ordered_bf16(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
+cudaError_t launch_ordered_i32(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
 }  // namespace ra
 
 namespace {
@@ -26,6 +33,11 @@ int elem_size(int dtype) {
     case RA_INT32: return 4;
     default: return 0;
   }
+}
+
+ra_status_t cuda_failed(cudaError_t err) {
+  g_last_cuda_error = (int)err;
+  return RA_ERR_CUDA;
 }
 
 struct Range {
@@ -78,7 +90,7 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
     }
   }
 
-  // 16-byte phases: the N-way side must share one phase for the vector path
+  // Address phases: the N-way side must share one phase for the vector path
   // (AR: all sources and destinations; RS: the sources; AG: the destinations).
   const Range* wide = kind == ra::KIND_ALLGATHER ? recv : send;
   const unsigned phase = (unsigned)(wide[0].lo % ra::kVecBytes);
@@ -107,28 +119,37 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
   a->vec_ok = same ? 1 : 0;
   a->inv_n = 1.0f / (float)nranks;
   a->step = 0;
+  a->acc32 = 0;
+  a->shape = ra::SHAPE_WIDE;
+  return RA_SUCCESS;
+}
+
+// SMs the launch may fill: all of them, or the caller's budget (max_sms > 0)
+// when other work runs beside the collective.
+ra_status_t sm_budget(int max_sms, int* sms) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return cuda_failed(err);
+  if (max_sms > 0 && max_sms < *sms) *sms = max_sms;
   return RA_SUCCESS;
 }
 
 // Grid: blockIdx.y = chunk (or rank, for the ring steps); blockIdx.x = CTAs
-// sharing it, enough to cover its vectors (per_thread of them per thread) but
-// no more than one resident wave in total.
-ra_status_t grid_for(const ra::Args& a, int dtype, int per_thread, dim3* grid) {
-  int dev = 0, sms = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (err != cudaSuccess) {
-    g_last_cuda_error = (int)err;
-    return RA_ERR_CUDA;
-  }
-  const int es = elem_size(dtype);
-  const uint64_t v = (uint64_t)(ra::kVecBytes / es);
+// sharing it, enough to cover its vectors but no more than one resident wave
+// of the launch shape on the SM budget.
+ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3* grid) {
+  int threads, per_thread, min_blocks, sms = 0;
+  ra::shape_params(shape, &threads, &per_thread, &min_blocks);
+  const ra_status_t st = sm_budget(max_sms, &sms);
+  if (st != RA_SUCCESS) return st;
+  const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
   const uint64_t n = (uint64_t)a.nranks;
   const uint64_t per_chunk = (a.count + n - 1) / n;
   const uint64_t work = a.vec_ok ? (per_chunk / v + 1) : per_chunk;  // vectors, or elements
-  const uint64_t per_cta = a.vec_ok ? (uint64_t)ra::kThreads * per_thread : (uint64_t)ra::kThreads;
+  const uint64_t per_cta = a.vec_ok ? (uint64_t)threads * per_thread : (uint64_t)threads;
   uint64_t gx = (work + per_cta - 1) / per_cta;
-  const uint64_t cap = (uint64_t)sms * ra::kMinBlocks / n;
+  const uint64_t cap = (uint64_t)sms * min_blocks / n;
   if (gx > cap) gx = cap;
   if (gx < 1) gx = 1;
   *grid = dim3((unsigned)gx, (unsigned)a.nranks);
@@ -145,27 +166,120 @@ ra_status_t launch(int kind, int dtype, int op, const ra::Args& a, dim3 grid, vo
     case RA_INT32: err = ra::launch_i32(kind, op, a, grid, s); break;
     default: return RA_ERR_UNSUPPORTED;
   }
-  if (err != cudaSuccess) {
-    g_last_cuda_error = (int)err;
-    return RA_ERR_CUDA;
-  }
-  return RA_SUCCESS;
+  return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
 }
 
-ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, size_t count,
-                ra_dtype_t dtype, ra_op_t op, int nranks, void* stream) {
+const ra_options_t kDefaultOptions = {RA_ORDER_RING, RA_ACCUM_DTYPE, 0};
+
+// ---- reduction programs of the other orders --------------------------------
+// A program is a list of steps slot[a] = op(slot[a], slot[b]) over the N rank
+// slots; after it runs, slot `root` holds the element's result.
+void emit(ra::OrderArgs& o, int pr, int a, int b) {
+  const int t = o.prog_len[pr]++;
+  o.prog[pr][t][0] = (uint8_t)a;
+  o.prog[pr][t][1] = (uint8_t)b;
+}
+
+// Recursive halving with distance d = N/2, ..., 1: the rank with the d bit
+// clear combines its partial (left operand) with its partner's, so level by
+// level slot r absorbs slot r + d.
+void rabenseifner_program(ra::OrderArgs& o, int pr, int n) {
+  for (int d = n / 2; d >= 1; d /= 2)
+    for (int r = 0; r < d; ++r) emit(o, pr, r, r + d);
+  o.root[pr] = 0;
+}
+
+// A binary tree laid over the rank sequence seq[lo..hi] in order (the middle
+// position is the root): a node folds its left subtree's partial, its own
+// value, then its right subtree's partial. Returns the slot of the result.
+int inorder_program(ra::OrderArgs& o, int pr, const int* seq, int lo, int hi) {
+  if (lo > hi) return -1;
+  const int m = (lo + hi) / 2, v = seq[m];
+  const int left = inorder_program(o, pr, seq, lo, m - 1);
+  const int right = inorder_program(o, pr, seq, m + 1, hi);
+  int acc = v;
+  if (left >= 0) {
+    emit(o, pr, left, v);
+    acc = left;
+  }
+  if (right >= 0) emit(o, pr, acc, right);
+  return acc;
+}
+
+// Double binary tree: tree 0 over ranks 0..N-1 reduces chunks [0, N/2),
+// tree 1 over ranks N-1..0 reduces the rest.
+void tree_programs(ra::OrderArgs& o, int n) {
+  int fwd[RA_MAX_RANKS], bwd[RA_MAX_RANKS];
+  for (int i = 0; i < n; ++i) {
+    fwd[i] = i;
+    bwd[i] = n - 1 - i;
+  }
+  o.root[0] = (uint8_t)inorder_program(o, 0, fwd, 0, n - 1);
+  o.root[1] = (uint8_t)inorder_program(o, 1, bwd, 0, n - 1);
+  for (int c = n / 2; c < n; ++c) o.chunk_prog |= (uint64_t)1 << c;
+}
+
+ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int order, int max_sms, void* stream) {
+  ra::OrderArgs o;
+  memset(&o, 0, sizeof(o));
+  o.base = a;
+  const int n = a.nranks;
+  if (order == RA_ORDER_RABENSEIFNER) rabenseifner_program(o, 0, n);
+  else tree_programs(o, n);
+  int sms = 0;
+  const ra_status_t st = sm_budget(max_sms, &sms);
+  if (st != RA_SUCCESS) return st;
+  // resident CTAs per SM: shared memory (N slots per thread) and at most 1024 threads
+  const uint64_t smem = (uint64_t)n * ra::kOrdThreads * ra::kVecBytes;
+  uint64_t per_sm = (uint64_t)(220 * 1024) / smem;
+  if (per_sm > 1024 / ra::kOrdThreads) per_sm = 1024 / ra::kOrdThreads;
+  if (per_sm < 1) per_sm = 1;
+  const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
+  const uint64_t per_chunk = (a.count + n - 1) / n;
+  const uint64_t work = a.vec_ok ? per_chunk / v + 1 : per_chunk;
+  uint64_t gx = (work + ra::kOrdThreads - 1) / ra::kOrdThreads;
+  const uint64_t cap = (uint64_t)sms * per_sm / (uint64_t)n;
+  if (gx > cap) gx = cap;
+  if (gx < 1) gx = 1;
+  const dim3 grid((unsigned)gx, (unsigned)n);
+  const bool is_rs = kind == ra::KIND_REDUCE_SCATTER;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  switch (dtype) {
+    case RA_FLOAT32: err = ra::launch_ordered_f32(is_rs, op, o, grid, s); break;
+    case RA_FLOAT16: err = ra::launch_ordered_f16(is_rs, op, o, grid, s); break;
+    case RA_BFLOAT16: err = ra::launch_ordered_bf16(is_rs, op, o, grid, s); break;
+    case RA_INT32: err = ra::launch_ordered_i32(is_rs, op, o, grid, s); break;
+    default: return RA_ERR_UNSUPPORTED;
+  }
+  return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
+}
+
+ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, size_t count, ra_dtype_t dtype,
+                ra_op_t op, int nranks, void* stream, const ra_options_t* options = &kDefaultOptions) {
   ra::Args a;
   if (kind == ra::KIND_ALLGATHER) op = RA_SUM;  // no reduction; any valid op is accepted
+  if (options == nullptr) options = &kDefaultOptions;
+  const int order = options->order, accum = options->accum, max_sms = options->max_sms;
+  if (accum != RA_ACCUM_DTYPE && accum != RA_ACCUM_FP32) return RA_ERR_INVALID_ARG;
+  if (order < RA_ORDER_RING || order > RA_ORDER_RABENSEIFNER || max_sms < 0) return RA_ERR_INVALID_ARG;
   ra_status_t st = prepare(kind, sendbufs, recvbufs, count, dtype, op, nranks, &a);
-  if (st != RA_SUCCESS || count == 0) return st;
+  if (st != RA_SUCCESS) return st;
+  if (order == RA_ORDER_RABENSEIFNER && (nranks & (nranks - 1))) return RA_ERR_UNSUPPORTED;
+  if (order != RA_ORDER_RING && accum == RA_ACCUM_FP32) return RA_ERR_UNSUPPORTED;
+  if (count == 0) return RA_SUCCESS;
+  if (order != RA_ORDER_RING) return run_ordered(kind, a, dtype, op, order, max_sms, stream);
+  a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
+  a.shape = kind == ra::KIND_ALLGATHER ? ra::SHAPE_STEP
+                                       : (nranks <= ra::kNarrowMaxRanks ? ra::SHAPE_NARROW : ra::SHAPE_WIDE);
   dim3 grid;
-  st = grid_for(a, dtype, ra::kUnroll, &grid);
+  st = grid_for(a, dtype, a.shape, max_sms, &grid);
   if (st != RA_SUCCESS) return st;
   return launch(kind, dtype, op, a, grid, stream);
 }
 
-ra_status_t run_ringsteps(const void* const* sendbufs, void* const* recvbufs, size_t count,
-                          ra_dtype_t dtype, ra_op_t op, int nranks, int nsteps, void* stream) {
+ra_status_t run_ringsteps(const void* const* sendbufs, void* const* recvbufs, size_t count, ra_dtype_t dtype,
+                          ra_op_t op, int nranks, int nsteps, void* stream) {
   ra::Args a;
   ra_status_t st = prepare(ra::KIND_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, nranks, &a);
   if (st != RA_SUCCESS || count == 0) return st;
@@ -173,15 +287,102 @@ ra_status_t run_ringsteps(const void* const* sendbufs, void* const* recvbufs, si
   if (nsteps < 0 || nsteps > total) nsteps = total;
   dim3 grid;
   if (nranks == 1) {  // no ring steps: the result is the (avg-scaled) copy
-    st = grid_for(a, dtype, ra::kUnroll, &grid);
+    a.shape = ra::SHAPE_NARROW;
+    st = grid_for(a, dtype, a.shape, 0, &grid);
     return st != RA_SUCCESS ? st : launch(ra::KIND_ALLREDUCE, dtype, op, a, grid, stream);
   }
-  st = grid_for(a, dtype, 1, &grid);
+  st = grid_for(a, dtype, ra::SHAPE_STEP, 0, &grid);
   if (st != RA_SUCCESS) return st;
   for (int k = 0; k < nsteps; ++k) {
     const bool rs = k < nranks - 1;
     a.step = rs ? k : k - (nranks - 1);
     st = launch(rs ? ra::KIND_RING_RS_STEP : ra::KIND_RING_AG_STEP, dtype, op, a, grid, stream);
+    if (st != RA_SUCCESS) return st;
+  }
+  return RA_SUCCESS;
+}
+
+// Gradient buckets (bitfern.com "AllReduce Explained", "PyTorch DDP and
+// Gradient Synchronization"; tirogla.com "Ring all-reduce", "Implementation
+// notes"): parameters are visited in the order backward produces their
+// gradients (reverse registration order) and packed into buckets of at most
+// bucket_bytes; a parameter larger than that gets a bucket of its own. With the
+// parameters laid out contiguously in registration order, every bucket is one
+// contiguous element range of the flat gradient buffer.
+ra_status_t bucket_plan(const size_t* counts, int nparams, size_t bucket_bytes, int elem_size_bytes,
+                        size_t* begin, size_t* count, int max_buckets, int* nbuckets) {
+  if (nparams < 0 || (nparams > 0 && counts == nullptr) || nbuckets == nullptr || bucket_bytes == 0 ||
+      (elem_size_bytes != 2 && elem_size_bytes != 4) || max_buckets < 0)
+    return RA_ERR_INVALID_ARG;
+  uint64_t end = 0;
+  for (int p = 0; p < nparams; ++p) end += counts[p];
+  int nb = 0;
+  uint64_t cur_begin = end, cur_bytes = 0;
+  bool open = false;
+  for (int p = nparams - 1; p >= 0; --p) {
+    const uint64_t bytes = (uint64_t)counts[p] * (uint64_t)elem_size_bytes;
+    if (open && cur_bytes + bytes > bucket_bytes) {  // close the current bucket
+      if (nb < max_buckets && begin && count) {
+        begin[nb] = (size_t)cur_begin;
+        count[nb] = (size_t)(end - cur_begin);
+      }
+      ++nb;
+      end = cur_begin;
+      cur_bytes = 0;
+      open = false;
+    }
+    cur_begin -= counts[p];
+    cur_bytes += bytes;
+    open = true;
+  }
+  if (open) {
+    if (nb < max_buckets && begin && count) {
+      begin[nb] = (size_t)cur_begin;
+      count[nb] = (size_t)(end - cur_begin);
+    }
+    ++nb;
+  }
+  *nbuckets = nb;
+  return nb <= max_buckets ? RA_SUCCESS : RA_ERR_INVALID_ARG;
+}
+
+ra_status_t run_buckets(const void* const* sendbufs, void* const* recvbufs, size_t count, ra_dtype_t dtype,
+                        ra_op_t op, int nranks, int nbuckets, const size_t* bucket_begin,
+                        const size_t* bucket_count, void* const* ready_events, const ra_options_t* options,
+                        void* stream) {
+  ra::Args whole;
+  ra_status_t st = prepare(ra::KIND_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, nranks, &whole);
+  if (st != RA_SUCCESS) return st;
+  if (nbuckets < 0 || (nbuckets > 0 && (bucket_begin == nullptr || bucket_count == nullptr)))
+    return RA_ERR_INVALID_ARG;
+  // buckets inside [0, count), disjoint, listed in ascending or descending order
+  int dir = 0;
+  for (int b = 0; b < nbuckets; ++b) {
+    if (bucket_begin[b] > count || bucket_count[b] > count - bucket_begin[b]) return RA_ERR_INVALID_ARG;
+    if (b > 0) {
+      const size_t pb = bucket_begin[b - 1], pe = pb + bucket_count[b - 1];
+      const size_t cb = bucket_begin[b], ce = cb + bucket_count[b];
+      const int d = cb >= pe ? 1 : (ce <= pb ? -1 : 0);
+      if (d == 0 || (dir != 0 && d != dir)) return RA_ERR_INVALID_ARG;
+      dir = d;
+    }
+  }
+  const int es = elem_size(dtype);
+  const void* s_ptr[RA_MAX_RANKS];
+  void* d_ptr[RA_MAX_RANKS];
+  for (int b = 0; b < nbuckets; ++b) {
+    if (ready_events && ready_events[b]) {
+      const cudaError_t err = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream),
+                                                  static_cast<cudaEvent_t>(ready_events[b]), 0);
+      if (err != cudaSuccess) return cuda_failed(err);
+    }
+    if (bucket_count[b] == 0) continue;
+    const size_t off = bucket_begin[b] * (size_t)es;
+    for (int r = 0; r < nranks; ++r) {
+      s_ptr[r] = static_cast<const char*>(sendbufs[r]) + off;
+      d_ptr[r] = static_cast<char*>(recvbufs[r]) + off;
+    }
+    st = run(ra::KIND_ALLREDUCE, s_ptr, d_ptr, bucket_count[b], dtype, op, nranks, stream, options);
     if (st != RA_SUCCESS) return st;
   }
   return RA_SUCCESS;
@@ -204,6 +405,31 @@ ra_status_t ra_reduce_scatter(const void* const* sendbufs, void* const* recvbufs
 ra_status_t ra_allgather(const void* const* sendbufs, void* const* recvbufs, size_t count,
                          ra_dtype_t dtype, ra_op_t op, int nranks, void* stream) {
   return run(ra::KIND_ALLGATHER, sendbufs, recvbufs, count, dtype, op, nranks, stream);
+}
+
+ra_status_t ra_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, size_t count, ra_dtype_t dtype,
+                            ra_op_t op, int nranks, const ra_options_t* options, void* stream) {
+  return run(ra::KIND_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, nranks, stream, options);
+}
+
+ra_status_t ra_reduce_scatter_ex(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                 ra_dtype_t dtype, ra_op_t op, int nranks, const ra_options_t* options,
+                                 void* stream) {
+  return run(ra::KIND_REDUCE_SCATTER, sendbufs, recvbufs, count, dtype, op, nranks, stream, options);
+}
+
+ra_status_t ra_bucket_plan(const size_t* param_counts, int nparams, size_t bucket_bytes, int elem_size,
+                           size_t* bucket_begin, size_t* bucket_count, int max_buckets, int* nbuckets) {
+  return bucket_plan(param_counts, nparams, bucket_bytes, elem_size, bucket_begin, bucket_count, max_buckets,
+                     nbuckets);
+}
+
+ra_status_t ra_allreduce_buckets(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                 ra_dtype_t dtype, ra_op_t op, int nranks, int nbuckets, const size_t* bucket_begin,
+                                 const size_t* bucket_count, void* const* ready_events,
+                                 const ra_options_t* options, void* stream) {
+  return run_buckets(sendbufs, recvbufs, count, dtype, op, nranks, nbuckets, bucket_begin, bucket_count,
+                     ready_events, options, stream);
 }
 
 ra_status_t ra_allreduce_ringsteps(const void* const* sendbufs, void* const* recvbufs, size_t count,
@@ -238,7 +464,7 @@ const char* ra_status_string(ra_status_t status) {
   switch (status) {
     case RA_SUCCESS: return "success";
     case RA_ERR_INVALID_ARG: return "invalid argument";
-    case RA_ERR_UNSUPPORTED: return "unsupported dtype/op";
+    case RA_ERR_UNSUPPORTED: return "unsupported dtype/op/order";
     case RA_ERR_ALIAS: return "buffers overlap outside the in-place layout";
     case RA_ERR_CUDA: return "CUDA launch failed";
   }
@@ -246,5 +472,7 @@ const char* ra_status_string(ra_status_t status) {
 }
 
 int ra_last_cuda_error(void) { return g_last_cuda_error; }
+
+int ra_vector_bytes(void) { return ra::kVecBytes; }
 
 }  // extern "C"

@@ -12,11 +12,12 @@
 // all-reduce N*S read + N*S written, reduce-scatter N*S + S, all-gather S + N*S.
 //
 // Work mapping: blockIdx.y = chunk c, so every CTA of a row folds in the same
-// rank order and derives the chunk's bounds once; blockIdx.x strides over the
-// chunk's 16-byte vectors (kUnroll vectors per thread per trip, loads of up to
-// kBatch ranks issued back to back before they are folded). The at most 2(V-1)
-// elements at the ends of each chunk, and every element when the buffers do
-// not share a 16-byte phase, go through the per-element path.
+// rank order and derives the chunk's bounds once; blockIdx.x splits the
+// chunk's vectors among the row's CTAs (the shape's kUnroll vectors per thread
+// per trip, loads of up to kBatch ranks issued back to back before they are
+// folded). The at most 2(V-1) elements at the ends of each chunk, and every
+// element when the buffers do not share one address phase, go through the
+// per-element path.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -31,24 +32,59 @@
 
 namespace ra {
 
-// Launch shape (build-time overridable for tuning sweeps; these defaults are the
-// measured choice on GB300).
-#ifndef RA_THREADS
-#define RA_THREADS 256
+// Launch shapes. The fused AR/RS kernels come in two shapes and the host
+// planner picks one from the rank count: with many ranks a thread already has
+// N loads per vector in flight, so few wide threads (4 vectors each, one CTA
+// per SM) keep HBM busiest; with few ranks more threads per SM are needed.
+// Measured on GB300 (8 x 256 MiB fp32: 97% of the copy bandwidth with the wide
+// shape against 94% with 512 threads x 2 vectors; 4 x 1 GiB fp32: 97% with the
+// narrow shape against 87% with the wide one). Build-time overridable for
+// tuning sweeps.
+#ifndef RA_WIDE_THREADS
+#define RA_WIDE_THREADS 256
 #endif
-#ifndef RA_MIN_BLOCKS
-#define RA_MIN_BLOCKS 2
+#ifndef RA_WIDE_MIN_BLOCKS
+#define RA_WIDE_MIN_BLOCKS 1
 #endif
-#ifndef RA_UNROLL
-#define RA_UNROLL 2
+#ifndef RA_WIDE_UNROLL
+#define RA_WIDE_UNROLL 4
 #endif
-#ifndef RA_BATCH
-#define RA_BATCH 8
+#ifndef RA_WIDE_BATCH
+#define RA_WIDE_BATCH 8
 #endif
-constexpr int kThreads = RA_THREADS;       // threads per CTA
-constexpr int kMinBlocks = RA_MIN_BLOCKS;  // resident CTAs per SM the register budget is set for
-constexpr int kUnroll = RA_UNROLL;         // 16-byte vectors per thread per trip
-constexpr int kBatch = RA_BATCH;           // ranks whose loads are in flight together
+#ifndef RA_NARROW_THREADS
+#define RA_NARROW_THREADS 256
+#endif
+#ifndef RA_NARROW_MIN_BLOCKS
+#define RA_NARROW_MIN_BLOCKS 3
+#endif
+#ifndef RA_NARROW_UNROLL
+#define RA_NARROW_UNROLL 1
+#endif
+#ifndef RA_NARROW_BATCH
+#define RA_NARROW_BATCH 4
+#endif
+#ifndef RA_NARROW_MAX_RANKS
+#define RA_NARROW_MAX_RANKS 5
+#endif
+// 0: the CTAs of a chunk interleave (grid-stride); 1: each CTA streams one
+// contiguous slab of the chunk.
+#ifndef RA_SCHEDULE
+#define RA_SCHEDULE 0
+#endif
+
+template <int THREADS, int MIN_BLOCKS, int UNROLL, int BATCH>
+struct Shape {
+  static constexpr int kThreads = THREADS;       // threads per CTA
+  static constexpr int kMinBlocks = MIN_BLOCKS;  // resident CTAs per SM the registers are budgeted for
+  static constexpr int kUnroll = UNROLL;         // vectors per thread per trip
+  static constexpr int kBatch = BATCH;           // ranks whose loads are in flight together
+};
+using WideShape = Shape<RA_WIDE_THREADS, RA_WIDE_MIN_BLOCKS, RA_WIDE_UNROLL, RA_WIDE_BATCH>;
+using NarrowShape = Shape<RA_NARROW_THREADS, RA_NARROW_MIN_BLOCKS, RA_NARROW_UNROLL, RA_NARROW_BATCH>;
+using StepShape = Shape<256, 2, 1, 1>;  // ring-step and all-gather kernels
+enum ShapeId { SHAPE_WIDE = 0, SHAPE_NARROW = 1, SHAPE_STEP = 2 };
+constexpr int kNarrowMaxRanks = RA_NARROW_MAX_RANKS;
 
 enum Kind {
   KIND_ALLREDUCE = 0,       // fused: one launch per call
@@ -63,20 +99,41 @@ struct Args {
   const void* src[RA_MAX_RANKS];
   void* dst[RA_MAX_RANKS];
   uint64_t count;            // elements per rank (the full vector length L)
-  uint64_t compact_aligned;  // bit c: the compact buffer of chunk c shares the 16-byte phase
+  uint64_t compact_aligned;  // bit c: the compact buffer of chunk c shares the vector phase
   int nranks;
-  int head;    // first element index on the common 16-byte grid, in [0, V)
+  int head;    // first element index on the common vector grid, in [0, V)
   int vec_ok;  // the N-way side (AR/RS: sources and AR destinations; AG: destinations) shares one phase
   float inv_n; // 1.0f / nranks, rounded in fp32
   int step;    // ring step of a KIND_RING_* launch
+  int acc32;   // fp16/bf16: partials stay in fp32 and are rounded once
+  int shape;   // ShapeId of the fused AR/RS launch
 };
+
+// The vectors [jbeg, jend) of a chunk this CTA handles, visited by its threads
+// from jbeg + threadIdx.x in strides of jstride (kUnroll vectors kThreads apart
+// per trip).
+struct Span {
+  uint64_t jbeg, jend, jstride;
+};
+template <class SH>
+__device__ __forceinline__ Span cta_span(uint64_t nv) {
+  constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
+#if RA_SCHEDULE == 0
+  return {(uint64_t)blockIdx.x * kThreads * kUnroll, nv, (uint64_t)gridDim.x * kThreads * kUnroll};
+#else
+  const uint64_t trip = (uint64_t)kThreads * kUnroll;
+  const uint64_t per = ((nv + gridDim.x - 1) / gridDim.x + trip - 1) / trip * trip;
+  const uint64_t b = (uint64_t)blockIdx.x * per;
+  return {b, b + per < nv ? b + per : nv, trip};
+#endif
+}
 
 // ---------------------------------------------------------------------------
 // the ring fold of kUnroll vectors at byte offsets off[] of every source
 // ---------------------------------------------------------------------------
-template <int DT, int OP>
+template <int DT, int OP, int kUnroll, int kBatch>
 __device__ __forceinline__ void fold_vectors(const Args& a, int c, int n, const uint64_t (&off)[kUnroll],
-                                             const bool (&ok)[kUnroll], uint4 (&acc)[kUnroll]) {
+                                             const bool (&ok)[kUnroll], Vec (&acc)[kUnroll]) {
   {
     const char* p = static_cast<const char*>(a.src[c]);
 #pragma unroll
@@ -84,7 +141,7 @@ __device__ __forceinline__ void fold_vectors(const Args& a, int c, int n, const 
       if (ok[u]) acc[u] = ld_vec(p + off[u]);
   }
   for (int k0 = 1; k0 < n; k0 += kBatch) {
-    uint4 x[kBatch][kUnroll];
+    Vec x[kBatch][kUnroll];
 #pragma unroll
     for (int kb = 0; kb < kBatch; ++kb) {
       const int k = k0 + kb;
@@ -111,21 +168,82 @@ __device__ __forceinline__ void fold_vectors(const Args& a, int c, int n, const 
   }
 }
 
-// the ring fold of one element i of chunk c
-template <int DT, int OP>
-__device__ __forceinline__ uint32_t fold_elem(const Args& a, int c, int n, uint64_t i) {
-  uint32_t acc = ld_elem<DT>(a.src[c], i);
-  for (int k = 1; k < n; ++k) {
-    int r = c + k;
-    if (r >= n) r -= n;
-    acc = elem_hop<DT, OP>(acc, ld_elem<DT>(a.src[r], i));
+// The same fold with fp32 partials for fp16/bf16 buffers (one rounding at the end).
+template <int DT, int OP, int kUnroll, int kBatch>
+__device__ __forceinline__ void fold_vectors_acc32(const Args& a, int c, int n, const uint64_t (&off)[kUnroll],
+                                                   const bool (&ok)[kUnroll], Vec (&out)[kUnroll]) {
+  VecF acc[kUnroll];
+  {
+    const char* p = static_cast<const char*>(a.src[c]);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (ok[u]) acc[u] = vec_widen<DT>(ld_vec(p + off[u]));
   }
-  if constexpr (OP == OP_AVG) acc = elem_avg<DT>(acc, a.inv_n, n);
-  return acc;
+  for (int k0 = 1; k0 < n; k0 += kBatch) {
+    Vec x[kBatch][kUnroll];
+#pragma unroll
+    for (int kb = 0; kb < kBatch; ++kb) {
+      const int k = k0 + kb;
+      if (k < n) {
+        int r = c + k;
+        if (r >= n) r -= n;
+        const char* p = static_cast<const char*>(a.src[r]);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          if (ok[u]) x[kb][u] = ld_vec(p + off[u]);
+      }
+    }
+#pragma unroll
+    for (int kb = 0; kb < kBatch; ++kb) {
+      if (k0 + kb < n) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) acc[u] = vecf_hop<OP>(acc[u], vec_widen<DT>(x[kb][u]));
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    if constexpr (OP == OP_AVG) {
+#pragma unroll
+      for (int k = 0; k < kVecHalves; ++k) acc[u].f[k] = __fmul_rn(acc[u].f[k], a.inv_n);
+    }
+    out[u] = vec_narrow<DT>(acc[u]);
+  }
+}
+
+template <int DT, int OP, bool ACC32, int kUnroll, int kBatch>
+__device__ __forceinline__ void fold(const Args& a, int c, int n, const uint64_t (&off)[kUnroll],
+                                     const bool (&ok)[kUnroll], Vec (&acc)[kUnroll]) {
+  if constexpr (ACC32) fold_vectors_acc32<DT, OP, kUnroll, kBatch>(a, c, n, off, ok, acc);
+  else fold_vectors<DT, OP, kUnroll, kBatch>(a, c, n, off, ok, acc);
+}
+
+// the ring fold of one element i of chunk c
+template <int DT, int OP, bool ACC32>
+__device__ __forceinline__ uint32_t fold_elem(const Args& a, int c, int n, uint64_t i) {
+  if constexpr (ACC32) {
+    float acc = widen16<DT>(ld_elem<DT>(a.src[c], i));
+    for (int k = 1; k < n; ++k) {
+      int r = c + k;
+      if (r >= n) r -= n;
+      acc = f32_hop<OP>(acc, widen16<DT>(ld_elem<DT>(a.src[r], i)));
+    }
+    if constexpr (OP == OP_AVG) acc = __fmul_rn(acc, a.inv_n);
+    return round16<DT>(acc);
+  } else {
+    uint32_t acc = ld_elem<DT>(a.src[c], i);
+    for (int k = 1; k < n; ++k) {
+      int r = c + k;
+      if (r >= n) r -= n;
+      acc = elem_hop<DT, OP>(acc, ld_elem<DT>(a.src[r], i));
+    }
+    if constexpr (OP == OP_AVG) acc = elem_avg<DT>(acc, a.inv_n, n);
+    return acc;
+  }
 }
 
 // Per-element path over [b0, vb) and [ve, b1), shared by the chunk's CTAs.
-template <typename F>
+template <int kThreads, typename F>
 __device__ __forceinline__ void for_each_edge_elem(uint64_t b0, uint64_t vb, uint64_t ve, uint64_t b1, F&& f) {
   const uint64_t n_lo = vb - b0, total = n_lo + (b1 - ve);
   for (uint64_t k = (uint64_t)blockIdx.x * kThreads + threadIdx.x; k < total;
@@ -137,27 +255,27 @@ __device__ __forceinline__ void for_each_edge_elem(uint64_t b0, uint64_t vb, uin
 // ---------------------------------------------------------------------------
 // all-reduce: every destination receives the fold
 // ---------------------------------------------------------------------------
-template <int DT, int OP>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) ar_fused_kernel(const __grid_constant__ Args a) {
+template <int DT, int OP, bool ACC32, class SH>
+__global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(const __grid_constant__ Args a) {
+  constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   const int n = a.nranks, c = blockIdx.y;
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
-  const uint64_t nv = (ve - vb) / V;
-  const uint64_t stride = (uint64_t)gridDim.x * kThreads * kUnroll;
-  for (uint64_t j0 = (uint64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; j0 < nv; j0 += stride) {
+  const Span sp = cta_span<SH>((ve - vb) / V);
+  for (uint64_t j0 = sp.jbeg + threadIdx.x; j0 < sp.jend; j0 += sp.jstride) {
     uint64_t off[kUnroll];
     bool ok[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint64_t j = j0 + (uint64_t)u * kThreads;
-      ok[u] = j < nv;
+      ok[u] = j < sp.jend;
       off[u] = (vb + j * V) * ES;
     }
-    uint4 acc[kUnroll];
-    fold_vectors<DT, OP>(a, c, n, off, ok, acc);
+    Vec acc[kUnroll];
+    fold<DT, OP, ACC32, kUnroll, SH::kBatch>(a, c, n, off, ok, acc);
     for (int r = 0; r < n; ++r) {
       char* q = static_cast<char*>(a.dst[r]);
 #pragma unroll
@@ -165,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) ar_fused_kernel(const __
         if (ok[u]) st_vec(q + off[u], acc[u]);
     }
   }
-  for_each_edge_elem(b0, vb, ve, b1, [&](uint64_t i) {
-    const uint32_t v = fold_elem<DT, OP>(a, c, n, i);
+  for_each_edge_elem<kThreads>(b0, vb, ve, b1, [&](uint64_t i) {
+    const uint32_t v = fold_elem<DT, OP, ACC32>(a, c, n, i);
     for (int r = 0; r < n; ++r) st_elem<DT>(a.dst[r], i, v);
   });
 }
@@ -174,29 +292,29 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) ar_fused_kernel(const __
 // ---------------------------------------------------------------------------
 // reduce-scatter: chunk c's fold goes to dst[c], compact (element i -> i - b0)
 // ---------------------------------------------------------------------------
-template <int DT, int OP>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) rs_fused_kernel(const __grid_constant__ Args a) {
+template <int DT, int OP, bool ACC32, class SH>
+__global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(const __grid_constant__ Args a) {
+  constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   const int n = a.nranks, c = blockIdx.y;
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
-  const uint64_t nv = (ve - vb) / V;
-  const uint64_t stride = (uint64_t)gridDim.x * kThreads * kUnroll;
+  const Span sp = cta_span<SH>((ve - vb) / V);
   void* out = a.dst[c];
   const bool out_vec = (a.compact_aligned >> c) & 1u;
-  for (uint64_t j0 = (uint64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; j0 < nv; j0 += stride) {
+  for (uint64_t j0 = sp.jbeg + threadIdx.x; j0 < sp.jend; j0 += sp.jstride) {
     uint64_t off[kUnroll];
     bool ok[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint64_t j = j0 + (uint64_t)u * kThreads;
-      ok[u] = j < nv;
+      ok[u] = j < sp.jend;
       off[u] = (vb + j * V) * ES;
     }
-    uint4 acc[kUnroll];
-    fold_vectors<DT, OP>(a, c, n, off, ok, acc);
+    Vec acc[kUnroll];
+    fold<DT, OP, ACC32, kUnroll, SH::kBatch>(a, c, n, off, ok, acc);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       if (!ok[u]) continue;
@@ -209,49 +327,48 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) rs_fused_kernel(const __
       }
     }
   }
-  for_each_edge_elem(b0, vb, ve, b1, [&](uint64_t i) {
-    st_elem<DT>(out, i - b0, fold_elem<DT, OP>(a, c, n, i));
+  for_each_edge_elem<kThreads>(b0, vb, ve, b1, [&](uint64_t i) {
+    st_elem<DT>(out, i - b0, fold_elem<DT, OP, ACC32>(a, c, n, i));
   });
 }
 
 // ---------------------------------------------------------------------------
 // all-gather: src[c] (chunk c, compact) goes to every dst at [b0, b1)
 // ---------------------------------------------------------------------------
-template <int DT>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) ag_copy_kernel(const __grid_constant__ Args a) {
+template <int DT, class SH>
+__global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ag_copy_kernel(const __grid_constant__ Args a) {
+  constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   const int n = a.nranks, c = blockIdx.y;
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
-  const uint64_t nv = (ve - vb) / V;
-  const uint64_t stride = (uint64_t)gridDim.x * kThreads * kUnroll;
+  const Span sp = cta_span<SH>((ve - vb) / V);
   const void* in = a.src[c];
   const bool in_vec = (a.compact_aligned >> c) & 1u;
-  for (uint64_t j0 = (uint64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; j0 < nv; j0 += stride) {
+  for (uint64_t j0 = sp.jbeg + threadIdx.x; j0 < sp.jend; j0 += sp.jstride) {
     uint64_t off[kUnroll];
     bool ok[kUnroll];
-    uint4 v[kUnroll];
+    Vec v[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint64_t j = j0 + (uint64_t)u * kThreads;
-      ok[u] = j < nv;
+      ok[u] = j < sp.jend;
       off[u] = (vb + j * V) * ES;
       if (!ok[u]) continue;
       if (in_vec) {
         v[u] = ld_vec(static_cast<const char*>(in) + off[u] - b0 * ES);
       } else {
         const uint64_t i = off[u] / ES - b0;
-        uint32_t w[4];
-        if constexpr (ES == 4) {
 #pragma unroll
-          for (int l = 0; l < 4; ++l) w[l] = ld_elem<DT>(in, i + l);
-        } else {
-#pragma unroll
-          for (int l = 0; l < 4; ++l) w[l] = ld_elem<DT>(in, i + 2 * l) | (ld_elem<DT>(in, i + 2 * l + 1) << 16);
+        for (int k = 0; k < kVecWords; ++k) {
+          if constexpr (ES == 4) {
+            v[u].w[k] = ld_elem<DT>(in, i + k);
+          } else {
+            v[u].w[k] = ld_elem<DT>(in, i + 2 * k) | (ld_elem<DT>(in, i + 2 * k + 1) << 16);
+          }
         }
-        v[u] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     for (int r = 0; r < n; ++r) {
@@ -261,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) ag_copy_kernel(const __g
         if (ok[u]) st_vec(q + off[u], v[u]);
     }
   }
-  for_each_edge_elem(b0, vb, ve, b1, [&](uint64_t i) {
+  for_each_edge_elem<kThreads>(b0, vb, ve, b1, [&](uint64_t i) {
     const uint32_t x = ld_elem<DT>(in, i - b0);
     for (int r = 0; r < n; ++r) st_elem<DT>(a.dst[r], i, x);
   });
@@ -281,7 +398,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) ag_copy_kernel(const __g
 // all-gather step s: dst[r][C] = dst[r-1][C] with C = (r - s) mod N.
 // ---------------------------------------------------------------------------
 template <int DT, int OP>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) ring_rs_step_kernel(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(StepShape::kThreads, StepShape::kMinBlocks)
+    ring_rs_step_kernel(const __grid_constant__ Args a) {
+  constexpr int kThreads = StepShape::kThreads;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   const int n = a.nranks, r = blockIdx.y, s = a.step;
@@ -297,11 +416,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) ring_rs_step_kernel(cons
   const uint64_t nv = (ve - vb) / V;
   for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < nv; j += (uint64_t)gridDim.x * kThreads) {
     const uint64_t off = (vb + j * V) * ES;
-    uint4 v = vec_hop<DT, OP>(ld_vec(static_cast<const char*>(in) + off), ld_vec(static_cast<const char*>(own) + off));
+    Vec v = vec_hop<DT, OP>(ld_vec(static_cast<const char*>(in) + off), ld_vec(static_cast<const char*>(own) + off));
     if (finish) v = vec_avg<DT>(v, a.inv_n, n);
     st_vec(static_cast<char*>(out) + off, v);
   }
-  for_each_edge_elem(b0, vb, ve, b1, [&](uint64_t i) {
+  for_each_edge_elem<kThreads>(b0, vb, ve, b1, [&](uint64_t i) {
     uint32_t v = elem_hop<DT, OP>(ld_elem<DT>(in, i), ld_elem<DT>(own, i));
     if (finish) v = elem_avg<DT>(v, a.inv_n, n);
     st_elem<DT>(out, i, v);
@@ -309,7 +428,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) ring_rs_step_kernel(cons
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) ring_ag_step_kernel(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(StepShape::kThreads, StepShape::kMinBlocks)
+    ring_ag_step_kernel(const __grid_constant__ Args a) {
+  constexpr int kThreads = StepShape::kThreads;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   const int n = a.nranks, r = blockIdx.y, s = a.step;
@@ -325,39 +446,65 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) ring_ag_step_kernel(cons
     const uint64_t off = (vb + j * V) * ES;
     st_vec(static_cast<char*>(out) + off, ld_vec(static_cast<const char*>(in) + off));
   }
-  for_each_edge_elem(b0, vb, ve, b1, [&](uint64_t i) { st_elem<DT>(out, i, ld_elem<DT>(in, i)); });
+  for_each_edge_elem<kThreads>(b0, vb, ve, b1, [&](uint64_t i) { st_elem<DT>(out, i, ld_elem<DT>(in, i)); });
 }
 
 // ---------------------------------------------------------------------------
 // host-side launch for one dtype (instantiated once per dtype translation unit)
 // ---------------------------------------------------------------------------
+template <int DT, int OP, class SH>
+cudaError_t launch_shaped(int kind, const Args& a, dim3 grid, cudaStream_t s) {
+  const dim3 block(SH::kThreads);
+  constexpr bool kNarrow = DT == DT_F16 || DT == DT_BF16;
+  if (kind == KIND_ALLREDUCE) {
+    if (kNarrow && a.acc32) ar_fused_kernel<DT, OP, kNarrow, SH><<<grid, block, 0, s>>>(a);
+    else ar_fused_kernel<DT, OP, false, SH><<<grid, block, 0, s>>>(a);
+  } else {
+    if (kNarrow && a.acc32) rs_fused_kernel<DT, OP, kNarrow, SH><<<grid, block, 0, s>>>(a);
+    else rs_fused_kernel<DT, OP, false, SH><<<grid, block, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+template <int DT, int OP>
+cudaError_t launch_op(int kind, const Args& a, dim3 grid, cudaStream_t s) {
+  if (kind == KIND_RING_RS_STEP) {
+    ring_rs_step_kernel<DT, OP><<<grid, StepShape::kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+  if (a.shape == SHAPE_NARROW) return launch_shaped<DT, OP, NarrowShape>(kind, a, grid, s);
+  return launch_shaped<DT, OP, WideShape>(kind, a, grid, s);
+}
+
 template <int DT>
 cudaError_t launch_dtype(int kind, int op, const Args& a, dim3 grid, cudaStream_t s) {
-  const dim3 block(kThreads);
   if (kind == KIND_ALLGATHER) {
-    ag_copy_kernel<DT><<<grid, block, 0, s>>>(a);
+    ag_copy_kernel<DT, StepShape><<<grid, StepShape::kThreads, 0, s>>>(a);
     return cudaGetLastError();
   }
   if (kind == KIND_RING_AG_STEP) {
-    ring_ag_step_kernel<DT><<<grid, block, 0, s>>>(a);
+    ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
     return cudaGetLastError();
   }
-#define RA_LAUNCH_OP(OPV)                                                            \
-  case OPV:                                                                          \
-    if (kind == KIND_ALLREDUCE) ar_fused_kernel<DT, OPV><<<grid, block, 0, s>>>(a);  \
-    else if (kind == KIND_REDUCE_SCATTER) rs_fused_kernel<DT, OPV><<<grid, block, 0, s>>>(a); \
-    else ring_rs_step_kernel<DT, OPV><<<grid, block, 0, s>>>(a);                     \
-    break;
   switch (op) {
-    RA_LAUNCH_OP(OP_SUM)
-    RA_LAUNCH_OP(OP_AVG)
-    RA_LAUNCH_OP(OP_MIN)
-    RA_LAUNCH_OP(OP_MAX)
-    RA_LAUNCH_OP(OP_PROD)
+    case OP_SUM: return launch_op<DT, OP_SUM>(kind, a, grid, s);
+    case OP_AVG: return launch_op<DT, OP_AVG>(kind, a, grid, s);
+    case OP_MIN: return launch_op<DT, OP_MIN>(kind, a, grid, s);
+    case OP_MAX: return launch_op<DT, OP_MAX>(kind, a, grid, s);
+    case OP_PROD: return launch_op<DT, OP_PROD>(kind, a, grid, s);
     default: return cudaErrorInvalidValue;
   }
-#undef RA_LAUNCH_OP
-  return cudaGetLastError();
+}
+
+// Threads, unroll and resident CTAs per SM of a shape, for the host planner.
+inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) {
+  if (shape == SHAPE_WIDE) {
+    *threads = WideShape::kThreads, *unroll = WideShape::kUnroll, *min_blocks = WideShape::kMinBlocks;
+  } else if (shape == SHAPE_NARROW) {
+    *threads = NarrowShape::kThreads, *unroll = NarrowShape::kUnroll, *min_blocks = NarrowShape::kMinBlocks;
+  } else {
+    *threads = StepShape::kThreads, *unroll = StepShape::kUnroll, *min_blocks = StepShape::kMinBlocks;
+  }
 }
 
 }  // namespace ra

@@ -20,6 +20,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "ra_plan.h"
+
 namespace ra {
 
 enum Dtype { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_I32 = 3 };
@@ -28,7 +30,7 @@ enum Op { OP_SUM = 0, OP_AVG = 1, OP_MIN = 2, OP_MAX = 3, OP_PROD = 4 };
 template <int DT>
 struct Elem {
   static constexpr int kSize = (DT == DT_F16 || DT == DT_BF16) ? 2 : 4;
-  static constexpr int kPerVec = 16 / kSize;  // elements per 16-byte vector
+  static constexpr int kPerVec = kVecBytes / kSize;  // elements per vector
 };
 
 // ---- scalar helpers on storage bits (held in the low bits of a uint32) ----
@@ -111,7 +113,7 @@ __device__ __forceinline__ uint32_t elem_avg(uint32_t v, float inv_n, int n) {
   }
 }
 
-// ---- 16-byte vectors ------------------------------------------------------
+// ---- word-level ops (one fp32/int32 lane, or two fp16/bf16 lanes) ----------
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t word_hop(uint32_t a, uint32_t b) {
   if constexpr (DT == DT_F32 || DT == DT_I32) {
@@ -149,30 +151,90 @@ __device__ __forceinline__ uint32_t word_avg(uint32_t v, float inv_n, int n) {
   }
 }
 
+// A vector of kVecBytes (16, or 32 with the sm_100+ 256-bit accesses), held
+// as 32-bit words: fp32/int32 lanes are words, fp16/bf16 lanes are half-words
+// (lane l in word l/2, low half first).
+constexpr int kVecWords = kVecBytes / 4;
+struct __align__(16) Vec {
+  uint32_t w[kVecWords];
+};
+
 template <int DT, int OP>
-__device__ __forceinline__ uint4 vec_hop(uint4 a, uint4 b) {
-  return make_uint4(word_hop<DT, OP>(a.x, b.x), word_hop<DT, OP>(a.y, b.y),
-                    word_hop<DT, OP>(a.z, b.z), word_hop<DT, OP>(a.w, b.w));
+__device__ __forceinline__ Vec vec_hop(const Vec& a, const Vec& b) {
+  Vec r;
+#pragma unroll
+  for (int k = 0; k < kVecWords; ++k) r.w[k] = word_hop<DT, OP>(a.w[k], b.w[k]);
+  return r;
 }
 template <int DT>
-__device__ __forceinline__ uint4 vec_avg(uint4 v, float inv_n, int n) {
-  return make_uint4(word_avg<DT>(v.x, inv_n, n), word_avg<DT>(v.y, inv_n, n),
-                    word_avg<DT>(v.z, inv_n, n), word_avg<DT>(v.w, inv_n, n));
+__device__ __forceinline__ Vec vec_avg(const Vec& v, float inv_n, int n) {
+  Vec r;
+#pragma unroll
+  for (int k = 0; k < kVecWords; ++k) r.w[k] = word_avg<DT>(v.w[k], inv_n, n);
+  return r;
 }
 
-// lane l of a 16-byte vector, as storage bits
+// lane l of a vector, as storage bits
 template <int DT>
-__device__ __forceinline__ uint32_t vec_lane(const uint4& v, int l) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ uint32_t vec_lane(const Vec& v, int l) {
   if constexpr (Elem<DT>::kSize == 4) {
-    return w[l];
+    return v.w[l];
   } else {
-    return (w[l >> 1] >> ((l & 1) * 16)) & 0xffffu;
+    return (v.w[l >> 1] >> ((l & 1) * 16)) & 0xffffu;
   }
 }
 
+// ---- fp32 accumulation for fp16/bf16 buffers ----------------------------------
+// The partial of every lane stays in fp32 from hop to hop; it is rounded to
+// the dtype once, after the avg multiply (tirogla.com "Ring all-reduce",
+// "Implementation notes": accumulate bf16 in fp32 at large N).
+constexpr int kVecHalves = kVecBytes / 2;
+struct VecF {
+  float f[kVecHalves];
+};
+template <int DT>
+__device__ __forceinline__ VecF vec_widen(const Vec& v) {
+  VecF r;
+#pragma unroll
+  for (int k = 0; k < kVecWords; ++k) {
+    r.f[2 * k] = widen16<DT>(v.w[k] & 0xffffu);
+    r.f[2 * k + 1] = widen16<DT>(v.w[k] >> 16);
+  }
+  return r;
+}
+template <int DT>
+__device__ __forceinline__ Vec vec_narrow(const VecF& a) {
+  Vec r;
+#pragma unroll
+  for (int k = 0; k < kVecWords; ++k) {
+    const float2 p = make_float2(a.f[2 * k], a.f[2 * k + 1]);
+    if constexpr (DT == DT_F16) {
+      const __half2 h = __float22half2_rn(p);
+      r.w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+      const __nv_bfloat162 h = __float22bfloat162_rn(p);
+      r.w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+  return r;
+}
+template <int OP>
+__device__ __forceinline__ float f32_hop(float a, float b) {
+  if constexpr (OP == OP_SUM || OP == OP_AVG) return __fadd_rn(a, b);
+  else if constexpr (OP == OP_PROD) return __fmul_rn(a, b);
+  else if constexpr (OP == OP_MIN) return fminimum(a, b);
+  else return fmaximum(a, b);
+}
+template <int OP>
+__device__ __forceinline__ VecF vecf_hop(const VecF& a, const VecF& b) {
+  VecF r;
+#pragma unroll
+  for (int k = 0; k < kVecHalves; ++k) r.f[k] = f32_hop<OP>(a.f[k], b.f[k]);
+  return r;
+}
+
 // ---- global memory ----------------------------------------------------------
-// Streaming (evict-first) 16-byte loads and stores: every byte is touched once.
+// Streaming (evict-first) vector loads and stores: every byte is touched once.
 // RA_LD_MODE / RA_ST_MODE select other cache hints for tuning sweeps
 // (0 = evict-first streaming, 1 = default caching).
 #ifndef RA_LD_MODE
@@ -181,19 +243,41 @@ __device__ __forceinline__ uint32_t vec_lane(const uint4& v, int l) {
 #ifndef RA_ST_MODE
 #define RA_ST_MODE 0
 #endif
-__device__ __forceinline__ uint4 ld_vec(const void* p) {
 #if RA_LD_MODE == 0
-  return __ldcs(reinterpret_cast<const uint4*>(p));
+#define RA_LD_HINT ".cs"
 #else
-  return *reinterpret_cast<const uint4*>(p);
+#define RA_LD_HINT ""
 #endif
-}
-__device__ __forceinline__ void st_vec(void* p, uint4 v) {
 #if RA_ST_MODE == 0
-  __stcs(reinterpret_cast<uint4*>(p), v);
+#define RA_ST_HINT ".cs"
 #else
-  *reinterpret_cast<uint4*>(p) = v;
+#define RA_ST_HINT ""
 #endif
+
+__device__ __forceinline__ Vec ld_vec(const void* p) {
+  Vec v;
+  if constexpr (kVecWords == 4) {
+    asm volatile("ld.global" RA_LD_HINT ".v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+  } else {
+    asm volatile("ld.global" RA_LD_HINT ".v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                   "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+  }
+  return v;
+}
+__device__ __forceinline__ void st_vec(void* p, const Vec& v) {
+  if constexpr (kVecWords == 4) {
+    asm volatile("st.global" RA_ST_HINT ".v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+                 "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+  } else {
+    asm volatile("st.global" RA_ST_HINT ".v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+                 "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
+  }
 }
 template <int DT>
 __device__ __forceinline__ uint32_t ld_elem(const void* base, uint64_t i) {

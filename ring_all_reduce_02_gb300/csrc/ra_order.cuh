@@ -1,0 +1,138 @@
+// All-reduce / reduce-scatter in the association of another algorithm the
+// pages describe (tirogla.com "Ring all-reduce", "How it works", cost model):
+// Rabenseifner's recursive halving (power-of-two N) or the double binary tree.
+// On one GPU these move the same bytes as the ring; only the order in which
+// each element's N values are combined differs, and that order fixes the
+// rounding.
+//
+// The host planner turns the algorithm into a reduction program of N-1 steps
+// "slot[a] = op(slot[a], slot[b])" over the N rank slots (at most two
+// programs, chosen per chunk: the double binary tree reduces the first N/2
+// chunks with one tree and the rest with the other). Each thread stages the N
+// vectors of its element range into its own shared-memory slots with cp.async
+// (16-byte global-to-shared copies, no registers held while they fly), waits
+// for its own copies only, runs the program on its slots and stores the
+// result. No thread reads another thread's slots, so no CTA barrier is needed.
+#pragma once
+
+#include "ra_kernels.cuh"
+
+namespace ra {
+
+constexpr int kOrdThreads = 2048 / kVecBytes;  // 128 threads at 16-byte vectors
+constexpr int kMaxProgSteps = RA_MAX_RANKS - 1;
+
+struct OrderArgs {
+  Args base;
+  uint8_t prog[2][kMaxProgSteps][2];  // (a, b) per step
+  uint8_t prog_len[2];
+  uint8_t root[2];          // slot holding the result after the program
+  uint64_t chunk_prog;      // bit c: chunk c runs program 1, else program 0
+};
+
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t run_prog_elem(const OrderArgs& o, int pr, int n, uint64_t i) {
+  uint32_t v[RA_MAX_RANKS];
+  for (int r = 0; r < n; ++r) v[r] = ld_elem<DT>(o.base.src[r], i);
+  for (int t = 0; t < o.prog_len[pr]; ++t) {
+    const int a = o.prog[pr][t][0], b = o.prog[pr][t][1];
+    v[a] = elem_hop<DT, OP>(v[a], v[b]);
+  }
+  uint32_t acc = v[o.root[pr]];
+  if constexpr (OP == OP_AVG) acc = elem_avg<DT>(acc, o.base.inv_n, n);
+  return acc;
+}
+
+// IS_RS: reduce-scatter (chunk c to dst[c], compact) instead of all-reduce.
+template <int DT, int OP, bool IS_RS>
+__global__ void __launch_bounds__(kOrdThreads) ordered_kernel(const __grid_constant__ OrderArgs o) {
+  extern __shared__ __align__(128) uint8_t slots[];  // [rank][thread] vectors
+  constexpr int V = Elem<DT>::kPerVec;
+  constexpr int ES = Elem<DT>::kSize;
+  const Args& a = o.base;
+  const int n = a.nranks, c = blockIdx.y;
+  const int pr = (int)((o.chunk_prog >> c) & 1u);
+  const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
+  uint64_t vb = b0, ve = b0;
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  const uint64_t nv = (ve - vb) / V;
+  Vec* my = reinterpret_cast<Vec*>(slots) + threadIdx.x;  // slot r at my[r * kOrdThreads]
+  void* out = a.dst[c];
+  const bool out_vec = !IS_RS || ((a.compact_aligned >> c) & 1u);
+  for (uint64_t j = (uint64_t)blockIdx.x * kOrdThreads + threadIdx.x; j < nv;
+       j += (uint64_t)gridDim.x * kOrdThreads) {
+    const uint64_t off = (vb + j * V) * ES;
+    for (int r = 0; r < n; ++r) {
+      const char* g = static_cast<const char*>(a.src[r]) + off;
+#pragma unroll
+      for (int h = 0; h < kVecBytes / 16; ++h)
+        cp_async_16(reinterpret_cast<char*>(my + r * kOrdThreads) + 16 * h, g + 16 * h);
+    }
+    cp_async_wait_all();
+    for (int t = 0; t < o.prog_len[pr]; ++t) {
+      Vec* sa = my + o.prog[pr][t][0] * kOrdThreads;
+      const Vec* sb = my + o.prog[pr][t][1] * kOrdThreads;
+      *sa = vec_hop<DT, OP>(*sa, *sb);
+    }
+    Vec v = my[o.root[pr] * kOrdThreads];
+    if constexpr (OP == OP_AVG) v = vec_avg<DT>(v, a.inv_n, n);
+    if constexpr (IS_RS) {
+      if (out_vec) {
+        st_vec(static_cast<char*>(out) + off - b0 * ES, v);
+      } else {
+        const uint64_t i = off / ES - b0;
+#pragma unroll
+        for (int l = 0; l < V; ++l) st_elem<DT>(out, i + l, vec_lane<DT>(v, l));
+      }
+    } else {
+      for (int r = 0; r < n; ++r) st_vec(static_cast<char*>(a.dst[r]) + off, v);
+    }
+  }
+  const uint64_t n_lo = vb - b0, total = n_lo + (b1 - ve);
+  for (uint64_t k = (uint64_t)blockIdx.x * kOrdThreads + threadIdx.x; k < total;
+       k += (uint64_t)gridDim.x * kOrdThreads) {
+    const uint64_t i = k < n_lo ? b0 + k : ve + (k - n_lo);
+    const uint32_t v = run_prog_elem<DT, OP>(o, pr, n, i);
+    if constexpr (IS_RS) {
+      st_elem<DT>(out, i - b0, v);
+    } else {
+      for (int r = 0; r < n; ++r) st_elem<DT>(a.dst[r], i, v);
+    }
+  }
+}
+
+template <int DT, int OP>
+cudaError_t launch_ordered_op(bool is_rs, const OrderArgs& o, dim3 grid, cudaStream_t s) {
+  const size_t smem = (size_t)o.base.nranks * kOrdThreads * kVecBytes;
+  cudaError_t err;
+  if (is_rs) {
+    err = cudaFuncSetAttribute(ordered_kernel<DT, OP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    ordered_kernel<DT, OP, true><<<grid, kOrdThreads, smem, s>>>(o);
+  } else {
+    err = cudaFuncSetAttribute(ordered_kernel<DT, OP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    ordered_kernel<DT, OP, false><<<grid, kOrdThreads, smem, s>>>(o);
+  }
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_ordered_dtype(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s) {
+  switch (op) {
+    case OP_SUM: return launch_ordered_op<DT, OP_SUM>(is_rs, o, grid, s);
+    case OP_AVG: return launch_ordered_op<DT, OP_AVG>(is_rs, o, grid, s);
+    case OP_MIN: return launch_ordered_op<DT, OP_MIN>(is_rs, o, grid, s);
+    case OP_MAX: return launch_ordered_op<DT, OP_MAX>(is_rs, o, grid, s);
+    case OP_PROD: return launch_ordered_op<DT, OP_PROD>(is_rs, o, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ra

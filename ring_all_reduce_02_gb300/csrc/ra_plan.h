@@ -5,10 +5,10 @@
 // with floor division (tirogla.com "Ring all-reduce", section "Code"). The
 // library accepts count < 2^57, so c*count (c <= 64) never leaves 63 bits.
 //
-// Within a chunk, elements whose byte address lies on the common 16-byte grid
-// of all buffers are moved as 16-byte vectors: the grid is {head + k*V}, with
-// V = 16 / elem_size and head the first element index whose address is 16-byte
-// aligned. A chunk's vector part is the largest run of whole vectors inside it;
+// Within a chunk, elements whose byte address lies on the common kVecBytes grid
+// of all buffers are moved as whole vectors: the grid is {head + k*V}, with
+// V = kVecBytes / elem_size and head the first element index whose address is
+// kVecBytes-aligned. A chunk's vector part is the largest run of whole vectors inside it;
 // the at most 2(V-1) elements at its two ends take the per-element path.
 #pragma once
 
@@ -22,13 +22,18 @@
 
 namespace ra {
 
-constexpr int kVecBytes = 16;
+// Bytes per vector access: 16 (ld/st.global.v4.b32) or 32 (the 256-bit
+// ld/st.global.v8.b32 of sm_100 and later). Build-time choice.
+#ifndef RA_VEC_BYTES
+#define RA_VEC_BYTES 16
+#endif
+constexpr int kVecBytes = RA_VEC_BYTES;
 
 RA_HD uint64_t chunk_begin(int c, int n, uint64_t count) {
   return ((uint64_t)c * count) / (uint64_t)n;
 }
 
-// [vb, ve): whole 16-byte vectors of the grid {head + k*V} inside [b0, b1).
+// [vb, ve): whole vectors of the grid {head + k*V} inside [b0, b1).
 // vb == ve when the chunk holds no whole vector.
 RA_HD void vec_range(uint64_t b0, uint64_t b1, uint64_t head, uint64_t v, uint64_t* vb,
                      uint64_t* ve) {

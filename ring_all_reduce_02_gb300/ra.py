@@ -19,11 +19,24 @@ LIB_PATH = os.path.join(HERE, "libra.so")
 RA_SUCCESS, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_ALIAS, RA_ERR_CUDA = range(5)
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
 OP_CODES = {"sum": 0, "avg": 1, "min": 2, "max": 3, "prod": 4}
+ORDER_CODES = {"ring": 0, "tree": 1, "rabenseifner": 2}
+ACCUM_CODES = {"dtype": 0, "fp32": 1}
 RA_MAX_RANKS = 64
 
 # every symbol include/ra.h declares
-EXPORTS = ("ra_allreduce", "ra_reduce_scatter", "ra_allgather", "ra_allreduce_ringsteps", "ra_chunk_range",
-           "ra_plan_chunk", "ra_status_string", "ra_last_cuda_error")
+EXPORTS = ("ra_allreduce", "ra_reduce_scatter", "ra_allgather", "ra_allreduce_ex", "ra_reduce_scatter_ex",
+           "ra_bucket_plan", "ra_allreduce_buckets", "ra_allreduce_ringsteps", "ra_chunk_range", "ra_plan_chunk",
+           "ra_status_string", "ra_last_cuda_error", "ra_vector_bytes")
+
+
+class Options(ctypes.Structure):
+    """ra_options_t."""
+
+    _fields_ = [("order", ctypes.c_int), ("accum", ctypes.c_int), ("max_sms", ctypes.c_int)]
+
+
+def options(order: str = "ring", accum: str = "dtype", max_sms: int = 0) -> Options:
+    return Options(ORDER_CODES[order], ACCUM_CODES[accum], max_sms)
 
 
 class RaError(RuntimeError):
@@ -50,10 +63,19 @@ def lib() -> ctypes.CDLL:
             VP, SZ, I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
             PP = ctypes.POINTER(ctypes.c_void_p)
             PSZ = ctypes.POINTER(ctypes.c_size_t)
+            POPT = ctypes.POINTER(Options)
             for name in ("ra_allreduce", "ra_reduce_scatter", "ra_allgather"):
                 f = getattr(L, name)
                 f.argtypes = [PP, PP, SZ, I, I, I, VP]
                 f.restype = I
+            for name in ("ra_allreduce_ex", "ra_reduce_scatter_ex"):
+                f = getattr(L, name)
+                f.argtypes = [PP, PP, SZ, I, I, I, POPT, VP]
+                f.restype = I
+            L.ra_bucket_plan.argtypes = [PSZ, I, SZ, I, PSZ, PSZ, I, ctypes.POINTER(I)]
+            L.ra_bucket_plan.restype = I
+            L.ra_allreduce_buckets.argtypes = [PP, PP, SZ, I, I, I, I, PSZ, PSZ, PP, POPT, VP]
+            L.ra_allreduce_buckets.restype = I
             L.ra_allreduce_ringsteps.argtypes = [PP, PP, SZ, I, I, I, I, VP]
             L.ra_allreduce_ringsteps.restype = I
             L.ra_chunk_range.argtypes = [SZ, I, I, PSZ, PSZ]
@@ -64,6 +86,8 @@ def lib() -> ctypes.CDLL:
             L.ra_status_string.restype = ctypes.c_char_p
             L.ra_last_cuda_error.argtypes = []
             L.ra_last_cuda_error.restype = I
+            L.ra_vector_bytes.argtypes = []
+            L.ra_vector_bytes.restype = I
             _lib = L
     return _lib
 
@@ -100,30 +124,98 @@ def _check(tensors, what):
             raise ValueError(f"{what}: buffers must be contiguous")
 
 
+def _check_full(sendbufs, recvbufs, what):
+    _check(list(sendbufs) + list(recvbufs), what)
+    count = sendbufs[0].numel()
+    if any(t.numel() != count for t in list(sendbufs) + list(recvbufs)) or len(recvbufs) != len(sendbufs):
+        raise ValueError(f"{what}: N send and N recv buffers of one length")
+    return count
+
+
+def _chunk_len(count: int, n: int, c: int) -> int:
+    return (c + 1) * count // n - c * count // n
+
+
 def call(name: str, send_ptrs, recv_ptrs, count: int, dtype: int, op: int, nranks: int, stream: int) -> int:
-    """Raw C call with integer device pointers; returns the ra_status_t."""
+    """Raw C call with integer pointers; returns the ra_status_t."""
     f = getattr(lib(), name)
     return f(ptr_array(send_ptrs), ptr_array(recv_ptrs), count, dtype, op, nranks, ctypes.c_void_p(stream or None))
 
 
+def call_ex(name: str, send_ptrs, recv_ptrs, count: int, dtype: int, op: int, nranks: int, order: int,
+            accum: int, stream: int, max_sms: int = 0) -> int:
+    """Raw C call of ra_allreduce_ex / ra_reduce_scatter_ex; returns the ra_status_t."""
+    f = getattr(lib(), name)
+    opts = Options(order, accum, max_sms)
+    return f(ptr_array(send_ptrs), ptr_array(recv_ptrs), count, dtype, op, nranks, ctypes.byref(opts),
+             ctypes.c_void_p(stream or None))
+
+
 def ra_allreduce(sendbufs, recvbufs, op: str = "sum", stream=None) -> None:
     """All-reduce of N equal-length tensors into N tensors (recv may be send: in place)."""
-    _check(list(sendbufs) + list(recvbufs), "ra_allreduce")
-    count = sendbufs[0].numel()
-    if any(t.numel() != count for t in list(sendbufs) + list(recvbufs)) or len(recvbufs) != len(sendbufs):
-        raise ValueError("ra_allreduce: N send and N recv buffers of one length")
+    count = _check_full(sendbufs, recvbufs, "ra_allreduce")
     st = call("ra_allreduce", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
               dtype_code(sendbufs[0]), OP_CODES[op], len(sendbufs), _stream_ptr(stream))
     if st:
         raise RaError(st, "ra_allreduce")
 
 
+def ra_allreduce_ex(sendbufs, recvbufs, op: str = "sum", order: str = "ring", accum: str = "dtype",
+                    max_sms: int = 0, stream=None) -> None:
+    """All-reduce with a reduction order (ring | tree | rabenseifner), accumulation (dtype | fp32)
+    and an SM budget (0 = all SMs)."""
+    count = _check_full(sendbufs, recvbufs, "ra_allreduce_ex")
+    st = call_ex("ra_allreduce_ex", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
+                 dtype_code(sendbufs[0]), OP_CODES[op], len(sendbufs), ORDER_CODES[order], ACCUM_CODES[accum],
+                 _stream_ptr(stream), max_sms)
+    if st:
+        raise RaError(st, "ra_allreduce_ex")
+
+
+def ra_reduce_scatter(sendbufs, recvbufs, op: str = "sum", stream=None) -> None:
+    """Reduce-scatter: recvbufs[r] receives chunk r (compact) of the reduction."""
+    _check(list(sendbufs) + [t for t in recvbufs if t.numel()], "ra_reduce_scatter")
+    count, n = sendbufs[0].numel(), len(sendbufs)
+    for r, t in enumerate(recvbufs):
+        if t.numel() != _chunk_len(count, n, r):
+            raise ValueError(f"ra_reduce_scatter: recvbufs[{r}] must hold chunk {r}")
+    st = call("ra_reduce_scatter", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
+              dtype_code(sendbufs[0]), OP_CODES[op], n, _stream_ptr(stream))
+    if st:
+        raise RaError(st, "ra_reduce_scatter")
+
+
+def ra_reduce_scatter_ex(sendbufs, recvbufs, op: str = "sum", order: str = "ring", accum: str = "dtype",
+                         max_sms: int = 0, stream=None) -> None:
+    """Reduce-scatter with a reduction order, accumulation and SM budget; recvbufs[r] receives chunk r."""
+    _check(list(sendbufs) + [t for t in recvbufs if t.numel()], "ra_reduce_scatter_ex")
+    count, n = sendbufs[0].numel(), len(sendbufs)
+    for r, t in enumerate(recvbufs):
+        if t.numel() != _chunk_len(count, n, r):
+            raise ValueError(f"ra_reduce_scatter_ex: recvbufs[{r}] must hold chunk {r}")
+    st = call_ex("ra_reduce_scatter_ex", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs],
+                 count, dtype_code(sendbufs[0]), OP_CODES[op], n, ORDER_CODES[order], ACCUM_CODES[accum],
+                 _stream_ptr(stream), max_sms)
+    if st:
+        raise RaError(st, "ra_reduce_scatter_ex")
+
+
+def ra_allgather(sendbufs, recvbufs, stream=None) -> None:
+    """All-gather: sendbufs[r] is chunk r (compact); every recvbufs[r] receives all chunks."""
+    _check([t for t in sendbufs if t.numel()] + list(recvbufs), "ra_allgather")
+    count, n = recvbufs[0].numel(), len(recvbufs)
+    for r, t in enumerate(sendbufs):
+        if t.numel() != _chunk_len(count, n, r):
+            raise ValueError(f"ra_allgather: sendbufs[{r}] must hold chunk {r}")
+    st = call("ra_allgather", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
+              dtype_code(recvbufs[0]), OP_CODES["sum"], n, _stream_ptr(stream))
+    if st:
+        raise RaError(st, "ra_allgather")
+
+
 def ra_allreduce_ringsteps(sendbufs, recvbufs, op: str = "sum", nsteps: int = -1, stream=None) -> None:
     """The literal ring schedule, one launch per step (first ``nsteps`` of 2(N-1); -1 = all)."""
-    _check(list(sendbufs) + list(recvbufs), "ra_allreduce_ringsteps")
-    count = sendbufs[0].numel()
-    if any(t.numel() != count for t in list(sendbufs) + list(recvbufs)) or len(recvbufs) != len(sendbufs):
-        raise ValueError("ra_allreduce_ringsteps: N send and N recv buffers of one length")
+    count = _check_full(sendbufs, recvbufs, "ra_allreduce_ringsteps")
     st = lib().ra_allreduce_ringsteps(ptr_array([t.data_ptr() for t in sendbufs]),
                                       ptr_array([t.data_ptr() for t in recvbufs]), count,
                                       dtype_code(sendbufs[0]), OP_CODES[op], len(sendbufs), nsteps,
@@ -132,32 +224,40 @@ def ra_allreduce_ringsteps(sendbufs, recvbufs, op: str = "sum", nsteps: int = -1
         raise RaError(st, "ra_allreduce_ringsteps")
 
 
-def ra_reduce_scatter(sendbufs, recvbufs, op: str = "sum", stream=None) -> None:
-    """Reduce-scatter: recvbufs[r] receives chunk r (compact) of the reduction."""
-    _check(list(sendbufs) + [t for t in recvbufs if t.numel()], "ra_reduce_scatter")
-    count, n = sendbufs[0].numel(), len(sendbufs)
-    for r, t in enumerate(recvbufs):
-        b, e = ra_chunk_range(count, n, r)
-        if t.numel() != e - b:
-            raise ValueError(f"ra_reduce_scatter: recvbufs[{r}] must hold {e - b} elements")
-    st = call("ra_reduce_scatter", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
-              dtype_code(sendbufs[0]), OP_CODES[op], n, _stream_ptr(stream))
+def ra_bucket_plan(param_counts, bucket_bytes: int, elem_size: int):
+    """DDP-style buckets over a flat buffer: list of (begin, count) in the order they become ready."""
+    n = len(param_counts)
+    counts = (ctypes.c_size_t * max(n, 1))(*param_counts)
+    nb = ctypes.c_int()
+    st = lib().ra_bucket_plan(counts, n, bucket_bytes, elem_size, None, None, 0, ctypes.byref(nb))
+    if st and not (st == RA_ERR_INVALID_ARG and nb.value > 0):
+        raise RaError(st, "ra_bucket_plan")
+    m = nb.value
+    begin = (ctypes.c_size_t * max(m, 1))()
+    cnt = (ctypes.c_size_t * max(m, 1))()
+    st = lib().ra_bucket_plan(counts, n, bucket_bytes, elem_size, begin, cnt, m, ctypes.byref(nb))
     if st:
-        raise RaError(st, "ra_reduce_scatter")
+        raise RaError(st, "ra_bucket_plan")
+    return [(begin[b], cnt[b]) for b in range(m)]
 
 
-def ra_allgather(sendbufs, recvbufs, stream=None) -> None:
-    """All-gather: sendbufs[r] is chunk r (compact); every recvbufs[r] receives all chunks."""
-    _check([t for t in sendbufs if t.numel()] + list(recvbufs), "ra_allgather")
-    count, n = recvbufs[0].numel(), len(recvbufs)
-    for r, t in enumerate(sendbufs):
-        b, e = ra_chunk_range(count, n, r)
-        if t.numel() != e - b:
-            raise ValueError(f"ra_allgather: sendbufs[{r}] must hold {e - b} elements")
-    st = call("ra_allgather", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
-              dtype_code(recvbufs[0]), OP_CODES["sum"], n, _stream_ptr(stream))
+def ra_allreduce_buckets(sendbufs, recvbufs, buckets, op: str = "sum", ready_events=None, order: str = "ring",
+                         accum: str = "dtype", max_sms: int = 0, stream=None) -> None:
+    """All-reduce every bucket (begin, count) of the flat buffers, each after its ready event."""
+    count = _check_full(sendbufs, recvbufs, "ra_allreduce_buckets")
+    m = len(buckets)
+    begin = (ctypes.c_size_t * max(m, 1))(*[b for b, _ in buckets])
+    cnt = (ctypes.c_size_t * max(m, 1))(*[c for _, c in buckets])
+    events = None
+    if ready_events is not None:
+        events = ptr_array([int(e.cuda_event) if e is not None else 0 for e in ready_events])
+    opts = options(order, accum, max_sms)
+    st = lib().ra_allreduce_buckets(ptr_array([t.data_ptr() for t in sendbufs]),
+                                    ptr_array([t.data_ptr() for t in recvbufs]), count, dtype_code(sendbufs[0]),
+                                    OP_CODES[op], len(sendbufs), m, begin, cnt, events, ctypes.byref(opts),
+                                    ctypes.c_void_p(_stream_ptr(stream) or None))
     if st:
-        raise RaError(st, "ra_allgather")
+        raise RaError(st, "ra_allreduce_buckets")
 
 
 def ra_chunk_range(count: int, nranks: int, c: int) -> tuple[int, int]:
@@ -169,7 +269,7 @@ def ra_chunk_range(count: int, nranks: int, c: int) -> tuple[int, int]:
 
 
 def ra_plan_chunk(count: int, nranks: int, c: int, elem_size: int, phase_bytes: int):
-    """(begin, end, vec_begin, vec_end) of chunk c: which part takes the 16-byte vector path."""
+    """(begin, end, vec_begin, vec_end) of chunk c: which part takes the vector path."""
     out = [ctypes.c_size_t() for _ in range(4)]
     st = lib().ra_plan_chunk(count, nranks, c, elem_size, phase_bytes, *[ctypes.byref(o) for o in out])
     if st:
@@ -179,3 +279,7 @@ def ra_plan_chunk(count: int, nranks: int, c: int, elem_size: int, phase_bytes: 
 
 def ra_status_string(status: int) -> str:
     return lib().ra_status_string(status).decode()
+
+
+def ra_vector_bytes() -> int:
+    return lib().ra_vector_bytes()

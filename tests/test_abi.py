@@ -6,6 +6,8 @@ import ctypes
 import os
 import re
 
+import numpy as np
+
 import pytest
 
 from conftest import ROOT
@@ -42,12 +44,14 @@ def test_chunk_range_is_floor_definition(ra):
 
 @pytest.mark.parametrize("es", [2, 4])
 def test_plan_splits_each_chunk_exactly_once(ra, es):
-    v = 16 // es
+    vb_bytes = ra.ra_vector_bytes()
+    assert vb_bytes in (16, 32)
+    v = vb_bytes // es
     for n in (1, 2, 3, 5, 7, 8, 16, 64):
         for count in list(range(0, 70)) + [1003, 4096, 1_000_003]:
-            for phase in range(0, 16, es):
+            for phase in range(0, vb_bytes, es):
                 covered = 0
-                head = ((16 - phase) % 16) // es
+                head = ((vb_bytes - phase) % vb_bytes) // es
                 for c in range(n):
                     b, e, vb, ve = ra.ra_plan_chunk(count, n, c, es, phase)
                     assert (b, e) == (c * count // n, (c + 1) * count // n)
@@ -97,6 +101,20 @@ def test_invalid_arguments(ra, name):
     assert call(name, s, d, 0, 0, 0, 4, 0) == ra.RA_SUCCESS                   # nothing to do
     f = getattr(ra.lib(), name)
     assert f(None, ra.ptr_array(d), 10, 0, 0, 4, None) == ra.RA_ERR_INVALID_ARG
+
+
+def test_ex_options(ra):
+    s, d = bufs(4), bufs(4, base=BASE + 64 * MB)
+    for name in ("ra_allreduce_ex", "ra_reduce_scatter_ex"):
+        assert ra.call_ex(name, s, d, 1000, 0, 0, 4, 7, 0, 0) == ra.RA_ERR_INVALID_ARG   # order
+        assert ra.call_ex(name, s, d, 1000, 0, 0, 4, 0, 5, 0) == ra.RA_ERR_INVALID_ARG   # accum
+        assert ra.call_ex(name, s, d, 1000, 0, 0, 4, 0, 0, 0, max_sms=-1) == ra.RA_ERR_INVALID_ARG
+        assert ra.call_ex(name, s[:3], d[:3], 1000, 0, 0, 3, 2, 0, 0) == ra.RA_ERR_UNSUPPORTED  # halving, N=3
+        assert ra.call_ex(name, s, d, 1000, 2, 0, 4, 1, 1, 0) == ra.RA_ERR_UNSUPPORTED  # fp32 accum + tree
+        assert ra.call_ex(name, s, d, 0, 0, 0, 4, 0, 1, 0) == ra.RA_SUCCESS
+    # NULL options = defaults
+    f = ra.lib().ra_allreduce_ex
+    assert f(ra.ptr_array(s), ra.ptr_array(d), 0, 0, 0, 4, None, None) == ra.RA_SUCCESS
 
 
 def test_zero_length_shards_may_be_null(ra):
@@ -149,3 +167,63 @@ def test_product_path_has_no_fallback(ra, monkeypatch):
     monkeypatch.setattr(binding, "LIB_PATH", "/nonexistent/libra.so")
     with pytest.raises(RuntimeError, match="missing"):
         binding.lib()
+
+
+def _ddp_buckets(counts, cap_bytes, es):
+    """The DDP packing rule written out: reverse order, close a bucket before it would exceed the cap."""
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + c)
+    out, cur, cur_bytes = [], [], 0
+    for p in reversed(range(len(counts))):
+        if cur and cur_bytes + counts[p] * es > cap_bytes:
+            out.append((offs[cur[-1]], offs[cur[0] + 1] - offs[cur[-1]]))
+            cur, cur_bytes = [], 0
+        cur.append(p)
+        cur_bytes += counts[p] * es
+    if cur:
+        out.append((offs[cur[-1]], offs[cur[0] + 1] - offs[cur[-1]]))
+    return out
+
+
+def test_bucket_plan_gpt2_medium(ra):
+    from ring_all_reduce_02_gb300 import inputs
+
+    counts = [int(np.prod(s)) for _, s in inputs.gpt2_medium_param_shapes()]
+    cap = 25 * 1000 * 1000
+    plan = ra.ra_bucket_plan(counts, cap, 2)
+    assert plan == _ddp_buckets(counts, cap, 2)
+    # buckets tile the flat buffer from its end to its start, each within the cap unless it is one parameter
+    assert plan[0][0] + plan[0][1] == sum(counts) and plan[-1][0] == 0
+    for (b0, c0), (b1, c1) in zip(plan, plan[1:]):
+        assert b1 + c1 == b0
+    big = {c for c in counts if c * 2 > cap}
+    for b, c in plan:
+        assert c * 2 <= cap or c in big
+    assert len(plan) > 10
+
+
+def test_bucket_plan_edge_cases(ra):
+    assert ra.ra_bucket_plan([], 100, 4) == []
+    assert ra.ra_bucket_plan([10], 4, 4) == [(0, 10)]        # larger than the cap: its own bucket
+    assert ra.ra_bucket_plan([1, 1, 1, 1], 8, 4) == [(2, 2), (0, 2)]
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        counts = [int(x) for x in rng.integers(0, 50, size=rng.integers(1, 30))]
+        cap = int(rng.integers(1, 300))
+        assert ra.ra_bucket_plan(counts, cap, 4) == _ddp_buckets(counts, cap, 4)
+
+
+def test_bucketed_allreduce_checks_buckets(ra):
+    s, d = bufs(2), bufs(2, base=BASE + 64 * MB)
+    f = ra.lib().ra_allreduce_buckets
+    C = ctypes.c_size_t
+
+    def run(begins, counts):
+        m = len(begins)
+        return f(ra.ptr_array(s), ra.ptr_array(d), 1000, 0, 0, 2, m, (C * m)(*begins), (C * m)(*counts), None, None,
+                 None)
+
+    assert run([0, 400], [500, 100]) == ra.RA_ERR_INVALID_ARG      # overlapping
+    assert run([900], [200]) == ra.RA_ERR_INVALID_ARG              # past the end
+    assert run([0, 600, 300], [100, 100, 100]) == ra.RA_ERR_INVALID_ARG  # not monotonic

@@ -420,3 +420,161 @@ def test_ringsteps_intermediate_states(ra):
             c = (r - s - 1) % n if s < n - 1 else (r - (s - (n - 1))) % n
             b, e = oracle.chunk_range(length, n, c)
             assert (to_host(recvs[r], dtype)[b:e] == snaps[s, r, b:e]).all(), (k, r, c)
+
+
+# ---------------------------------------------------------------------------
+# fp32 accumulation (partials kept in fp32, rounded once) against the oracle's fp32-message ring
+# ---------------------------------------------------------------------------
+def _run_ex(ra, xs, op, dtype, order="ring", accum="dtype"):
+    sends = [to_device(x, dtype) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    ra.ra_allreduce_ex(sends, recvs, op, order=order, accum=accum)
+    n, length = len(xs), xs[0].size
+    shards = [torch.empty((c + 1) * length // n - c * length // n, dtype=TORCH_DTYPE[dtype], device="cuda")
+              for c in range(n)]
+    ra.ra_reduce_scatter_ex(sends, shards, op, order=order, accum=accum)
+    torch.cuda.synchronize()
+    return [to_host(r, dtype) for r in recvs], [to_host(s, dtype) for s in shards]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("op", OPS)
+def test_fp32_accumulation(ra, dtype, op):
+    for n, length in ((1, 100), (2, 1001), (3, 4097), (8, 65536 + 5), (16, 1003), (64, 64 * 33 + 1)):
+        xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=n + 17)
+        want, _ = oracle.allreduce_ex(xs, op, dtype, accum="fp32")
+        got, shards = _run_ex(ra, xs, op, dtype, accum="fp32")
+        for r in range(n):
+            assert_same_bits(got[r], want[r], dtype, f"n={n} L={length} rank {r}")
+            b, e = oracle.chunk_range(length, n, r)
+            assert_same_bits(shards[r], want[0][b:e], dtype, f"RS n={n} shard {r}")
+
+
+def test_fp32_accumulation_closed_form(ra):
+    # rank 0 holds 256, 63 ranks hold 1: per-hop bf16 rounding stalls chunk 0 at 256, fp32 partials give 320
+    n, length = 64, 64 * 64
+    xs = [np.full(length, 0x3F80, dtype=np.uint16) for _ in range(n)]
+    xs[0][:] = 0x4380
+    hop, _ = _run_ex(ra, xs, "sum", "bf16", accum="dtype")
+    acc, _ = _run_ex(ra, xs, "sum", "bf16", accum="fp32")
+    b0, e0 = oracle.chunk_range(length, n, 0)
+    assert (oracle.widen("bf16", hop[0][b0:e0]) == 256.0).all()
+    assert (oracle.widen("bf16", acc[7]) == 320.0).all()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_fp32_accumulation_is_identity_for_wide_types(ra, dtype):
+    xs = inputs.rank_buffers(5, 10_003, dtype, dist_for(dtype, "sum"), seed_base=3)
+    a, _ = _run_ex(ra, xs, "sum", dtype, accum="fp32")
+    b = run_allreduce(ra, xs, "sum", dtype)
+    assert all(x.tobytes() == y.tobytes() for x, y in zip(a, b))
+
+
+# ---------------------------------------------------------------------------
+# other reduction orders (double binary tree, Rabenseifner) against the oracle's
+# message-passing simulations of those algorithms
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("order", ["tree", "rabenseifner"])
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("f32", "avg"), ("bf16", "sum"), ("bf16", "avg"),
+                                      ("f16", "prod"), ("f16", "max"), ("i32", "sum"), ("i32", "min"),
+                                      ("bf16", "min"), ("f32", "prod")])
+def test_other_orders(ra, order, dtype, op):
+    ns = (1, 2, 4, 8, 16, 64) if order == "rabenseifner" else (1, 2, 3, 5, 7, 8, 16, 64)
+    for n in ns:
+        for length in (1, 13, 1003, 65536 + 7):
+            xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=n + length)
+            want, _ = oracle.allreduce_ex(xs, op, dtype, order=order)
+            got, shards = _run_ex(ra, xs, op, dtype, order=order)
+            for r in range(n):
+                assert_same_bits(got[r], want[r], dtype, f"{order} n={n} L={length} rank {r}")
+                b, e = oracle.chunk_range(length, n, r)
+                assert_same_bits(shards[r], want[0][b:e], dtype, f"{order} RS n={n} shard {r}")
+
+
+def test_other_orders_differ_from_ring_only_by_rounding(ra):
+    # same values, different association: fp32 results agree with the ring to 1e-6 relative
+    n, length = 8, 1 << 20
+    xs = inputs.rank_buffers(n, length, "f32", ("uniform", 0.5, 1.0), seed_base=1)
+    ring = run_allreduce(ra, xs, "sum", "f32")[0]
+    for order in ("tree", "rabenseifner"):
+        got, _ = _run_ex(ra, xs, "sum", "f32", order=order)
+        np.testing.assert_allclose(got[0], ring, rtol=1e-6)
+        assert not np.array_equal(got[0], ring)  # the order is observable
+
+
+def test_rabenseifner_rejects_non_power_of_two(ra):
+    xs = [torch.ones(10, device="cuda") for _ in range(3)]
+    with pytest.raises(ra.RaError):
+        ra.ra_allreduce_ex(xs, [torch.empty_like(x) for x in xs], "sum", order="rabenseifner")
+
+
+@pytest.mark.parametrize("order", ["tree", "rabenseifner"])
+def test_other_orders_full_size_sampled(ra, order):
+    n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_f32_avg_64m"]
+    xs = inputs.rank_buffers(n, length, dtype, dist)
+    sends = [to_device(x, dtype) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    ra.ra_allreduce_ex(sends, recvs, op, order=order)
+    torch.cuda.synchronize()
+    for r in range(1, n):
+        assert torch.equal(recvs[r], recvs[0])
+    idx = sample_indices(length, n, k=1 << 12)
+    got = to_host(recvs[0][torch.from_numpy(idx).cuda()], dtype)
+    # the association depends only on which tree reduces the element (tree: chunks below N/2 use
+    # tree 0), so the sampled columns are evaluated by the oracle laid out in a chunk of the same tree
+    split = (n // 2) * length // n
+    for half, mask in ((0, idx < split), (1, idx >= split)):
+        cols = [np.ascontiguousarray(x[idx][mask]) for x in xs]
+        m = cols[0].size
+        if not m:
+            continue
+        if order == "tree":
+            pad = [np.concatenate([c] * n) for c in cols]  # n chunks of m elements
+            want_all, _ = oracle.allreduce_ex(pad, op, dtype, order=order)
+            want = want_all[0][:m] if half == 0 else want_all[0][(n - 1) * m:]
+        else:
+            want_all, _ = oracle.allreduce_ex(cols, op, dtype, order=order)
+            want = want_all[0]
+        assert_same_bits(got[mask], want, dtype, f"{order} sampled half {half}")
+
+
+# ---------------------------------------------------------------------------
+# bucketed all-reduce (each bucket is its own all-reduce) and the SM budget
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("bf16", "avg"), ("i32", "max")])
+def test_bucketed_allreduce(ra, dtype, op):
+    counts = [1000, 3, 77, 4096, 10, 2048, 5, 65536, 1, 333]
+    n, length = 5, sum(counts)
+    es = ELEM_SIZE[dtype]
+    plan = ra.ra_bucket_plan(counts, 8000 * es, es)
+    assert len(plan) > 3
+    xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=11)
+    sends = [to_device(x, dtype) for x in xs]
+    recvs = [torch.zeros_like(s) for s in sends]
+    # gradients "become ready" on a producer stream; the collective waits on each bucket's event
+    producer = torch.cuda.Stream()
+    events = []
+    with torch.cuda.stream(producer):
+        for _ in plan:
+            torch.cuda._sleep(20000)
+            ev = torch.cuda.Event()
+            ev.record(producer)
+            events.append(ev)
+    ra.ra_allreduce_buckets(sends, recvs, plan, op, ready_events=events)
+    torch.cuda.synchronize()
+    for b, c in plan:
+        want, _, _ = oracle.allreduce([np.ascontiguousarray(x[b:b + c]) for x in xs], op, dtype)
+        for r in range(n):
+            assert_same_bits(to_host(recvs[r][b:b + c], dtype), want[r], dtype, f"bucket {b} rank {r}")
+
+
+def test_sm_budget_changes_nothing_but_speed(ra):
+    n, length = 8, (1 << 22) + 5
+    xs = inputs.rank_buffers(n, length, "bf16", ("normal", 1.0), seed_base=4)
+    base = run_allreduce(ra, xs, "avg", "bf16")
+    for max_sms in (1, 8, 76):
+        sends = [to_device(x, "bf16") for x in xs]
+        recvs = [torch.empty_like(s) for s in sends]
+        ra.ra_allreduce_ex(sends, recvs, "avg", max_sms=max_sms)
+        torch.cuda.synchronize()
+        assert all(to_host(r, "bf16").tobytes() == b.tobytes() for r, b in zip(recvs, base))
