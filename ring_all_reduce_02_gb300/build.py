@@ -1,6 +1,7 @@
 """Build libra.so in-tree for sm_103a with nvcc (no cmake, no torch extension).
 
-Each translation unit under csrc/ compiles in parallel; the objects link into
+Each translation unit under csrc/ compiles in parallel (the kernel slice
+source once per dtype and op); the objects link into
 ``ring_all_reduce_02_gb300/libra.so`` with the CUDA runtime linked statically,
 so the library loads without any search-path setup.
 
@@ -36,8 +37,23 @@ def _nvcc() -> str:
     return cand
 
 
-def sources() -> list[str]:
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+SLICE_SOURCE = "ra_launch_op.cu"  # compiled once per (dtype id, op id)
+SLICES = [(dt, op) for dt in range(4) for op in range(5)]
+
+
+def sources() -> list[tuple[str, str, list[str]]]:
+    """(source, object name, extra defines) for every compilation."""
+    out = []
+    for f in sorted(os.listdir(CSRC)):
+        if not f.endswith(".cu"):
+            continue
+        src = os.path.join(CSRC, f)
+        if f == SLICE_SOURCE:
+            for dt, op in SLICES:
+                out.append((src, f"ra_launch_op_{dt}_{op}.o", [f"-DRA_SLICE_DT={dt}", f"-DRA_SLICE_OP={op}"]))
+        else:
+            out.append((src, f[:-3] + ".o", []))
+    return out
 
 
 def _deps_newer(target: str) -> bool:
@@ -57,9 +73,10 @@ def build(force: bool = False, verbose: bool = False, defines=(), lib_path: str 
     os.makedirs(out_dir, exist_ok=True)
     extra = (["-Xptxas", "-v"] if verbose else []) + [f"-D{d}" for d in defines]
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+    def compile_one(job) -> str:
+        src, obj_name, slice_defs = job
+        obj = os.path.join(out_dir, obj_name)
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, *slice_defs, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -67,9 +84,9 @@ def build(force: bool = False, verbose: bool = False, defines=(), lib_path: str 
             sys.stderr.write(r.stderr)
         return obj
 
-    srcs = sources()
-    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_one, srcs))
+    jobs = sources()
+    with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, jobs))
     tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)

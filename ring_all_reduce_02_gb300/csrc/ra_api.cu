@@ -11,14 +11,8 @@
 #include "ra_order.cuh"
 
 namespace ra {
-cudaError_t launch_f32(int kind, int op, const Args& a, dim3 grid, cudaStream_t s);
-cudaError_t launch_f16(int kind, int op, const Args& a, dim3 grid, cudaStream_t s);
-cudaError_t launch_bf16(int kind, int op, const Args& a, dim3 grid, cudaStream_t s);
-cudaError_t launch_i32(int kind, int op, const Args& a, dim3 grid, cudaStream_t s);
-cudaError_t launch_ordered_f32(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
-cudaError_t launch_ordered_f16(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
-cudaError_t launch_ordered_bf16(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
-cudaError_t launch_ordered_i32(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
+cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid, cudaStream_t s);
+cudaError_t launch_ordered_kernel(bool is_rs, int dtype, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
 }  // namespace ra
 
 namespace {
@@ -120,7 +114,7 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
   a->inv_n = 1.0f / (float)nranks;
   a->step = 0;
   a->acc32 = 0;
-  a->shape = ra::SHAPE_WIDE;
+  a->shape = ra::shape_for(nranks);
   return RA_SUCCESS;
 }
 
@@ -157,15 +151,7 @@ ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3*
 }
 
 ra_status_t launch(int kind, int dtype, int op, const ra::Args& a, dim3 grid, void* stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t err;
-  switch (dtype) {
-    case RA_FLOAT32: err = ra::launch_f32(kind, op, a, grid, s); break;
-    case RA_FLOAT16: err = ra::launch_f16(kind, op, a, grid, s); break;
-    case RA_BFLOAT16: err = ra::launch_bf16(kind, op, a, grid, s); break;
-    case RA_INT32: err = ra::launch_i32(kind, op, a, grid, s); break;
-    default: return RA_ERR_UNSUPPORTED;
-  }
+  const cudaError_t err = ra::launch_kernel(kind, dtype, op, a, grid, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
 }
 
@@ -242,16 +228,8 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
   if (gx > cap) gx = cap;
   if (gx < 1) gx = 1;
   const dim3 grid((unsigned)gx, (unsigned)n);
-  const bool is_rs = kind == ra::KIND_REDUCE_SCATTER;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t err;
-  switch (dtype) {
-    case RA_FLOAT32: err = ra::launch_ordered_f32(is_rs, op, o, grid, s); break;
-    case RA_FLOAT16: err = ra::launch_ordered_f16(is_rs, op, o, grid, s); break;
-    case RA_BFLOAT16: err = ra::launch_ordered_bf16(is_rs, op, o, grid, s); break;
-    case RA_INT32: err = ra::launch_ordered_i32(is_rs, op, o, grid, s); break;
-    default: return RA_ERR_UNSUPPORTED;
-  }
+  const cudaError_t err = ra::launch_ordered_kernel(kind == ra::KIND_REDUCE_SCATTER, dtype, op, o, grid,
+                                                    static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
 }
 
@@ -271,7 +249,7 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   if (order != RA_ORDER_RING) return run_ordered(kind, a, dtype, op, order, max_sms, stream);
   a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
   a.shape = kind == ra::KIND_ALLGATHER ? ra::SHAPE_STEP
-                                       : (nranks <= ra::kNarrowMaxRanks ? ra::SHAPE_NARROW : ra::SHAPE_WIDE);
+                                       : ra::shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0);
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
   if (st != RA_SUCCESS) return st;
@@ -287,7 +265,7 @@ ra_status_t run_ringsteps(const void* const* sendbufs, void* const* recvbufs, si
   if (nsteps < 0 || nsteps > total) nsteps = total;
   dim3 grid;
   if (nranks == 1) {  // no ring steps: the result is the (avg-scaled) copy
-    a.shape = ra::SHAPE_NARROW;
+    a.shape = ra::shape_for(1);
     st = grid_for(a, dtype, a.shape, 0, &grid);
     return st != RA_SUCCESS ? st : launch(ra::KIND_ALLREDUCE, dtype, op, a, grid, stream);
   }

@@ -32,41 +32,15 @@
 
 namespace ra {
 
-// Launch shapes. The fused AR/RS kernels come in two shapes and the host
-// planner picks one from the rank count: with many ranks a thread already has
-// N loads per vector in flight, so few wide threads (4 vectors each, one CTA
-// per SM) keep HBM busiest; with few ranks more threads per SM are needed.
-// Measured on GB300 (8 x 256 MiB fp32: 97% of the copy bandwidth with the wide
-// shape against 94% with 512 threads x 2 vectors; 4 x 1 GiB fp32: 97% with the
-// narrow shape against 87% with the wide one). Build-time overridable for
-// tuning sweeps.
-#ifndef RA_WIDE_THREADS
-#define RA_WIDE_THREADS 256
-#endif
-#ifndef RA_WIDE_MIN_BLOCKS
-#define RA_WIDE_MIN_BLOCKS 1
-#endif
-#ifndef RA_WIDE_UNROLL
-#define RA_WIDE_UNROLL 4
-#endif
-#ifndef RA_WIDE_BATCH
-#define RA_WIDE_BATCH 8
-#endif
-#ifndef RA_NARROW_THREADS
-#define RA_NARROW_THREADS 256
-#endif
-#ifndef RA_NARROW_MIN_BLOCKS
-#define RA_NARROW_MIN_BLOCKS 3
-#endif
-#ifndef RA_NARROW_UNROLL
-#define RA_NARROW_UNROLL 1
-#endif
-#ifndef RA_NARROW_BATCH
-#define RA_NARROW_BATCH 4
-#endif
-#ifndef RA_NARROW_MAX_RANKS
-#define RA_NARROW_MAX_RANKS 5
-#endif
+// Launch shapes of the fused AR/RS kernels. How many bytes a thread keeps in
+// flight is N loads x kUnroll vectors, so the rank count decides how many
+// threads per SM and vectors per thread keep HBM busiest; the host planner
+// picks the shape from N. Measured on GB300 (fraction of the copy bandwidth,
+// fp32 all-reduce of 0.5-2 GiB per rank): N = 2: 98% with 128 threads x 2
+// vectors at 8 CTAs/SM (88% with the N = 4 shape); N = 3 and 4: 90% and 97%
+// with 256 x 8 at 1 CTA/SM; N = 5: 87% with 256 x 2 at 2 CTAs/SM; N = 6..11:
+// 256 x 4 at 1 CTA/SM with loads of 8 ranks in flight (98% at N = 8); N >= 12:
+// the same with batches of 4 ranks (97% at N = 16 against 95%).
 // 0: the CTAs of a chunk interleave (grid-stride); 1: each CTA streams one
 // contiguous slab of the chunk.
 #ifndef RA_SCHEDULE
@@ -80,11 +54,27 @@ struct Shape {
   static constexpr int kUnroll = UNROLL;         // vectors per thread per trip
   static constexpr int kBatch = BATCH;           // ranks whose loads are in flight together
 };
-using WideShape = Shape<RA_WIDE_THREADS, RA_WIDE_MIN_BLOCKS, RA_WIDE_UNROLL, RA_WIDE_BATCH>;
-using NarrowShape = Shape<RA_NARROW_THREADS, RA_NARROW_MIN_BLOCKS, RA_NARROW_UNROLL, RA_NARROW_BATCH>;
+using ShapeN2 = Shape<128, 8, 2, 4>;    // nranks 1..2
+using ShapeN4 = Shape<256, 1, 8, 4>;    // nranks 3..4
+using ShapeN5 = Shape<256, 2, 2, 4>;    // nranks 5
+using ShapeW8 = Shape<256, 1, 4, 8>;    // nranks 6..11
+using ShapeW16 = Shape<256, 1, 4, 4>;   // nranks 12..64
 using StepShape = Shape<256, 2, 1, 1>;  // ring-step and all-gather kernels
-enum ShapeId { SHAPE_WIDE = 0, SHAPE_NARROW = 1, SHAPE_STEP = 2 };
-constexpr int kNarrowMaxRanks = RA_NARROW_MAX_RANKS;
+enum ShapeId { SHAPE_N2 = 0, SHAPE_N4 = 1, SHAPE_N5 = 2, SHAPE_W8 = 3, SHAPE_W16 = 4, SHAPE_STEP = 5 };
+
+// The fused shape for a call. Reduce-scatter writes one compact chunk instead
+// of N copies and does best with the N = 2 shape up to N = 4 (103% of the copy
+// bandwidth at N = 4); fp32 accumulation at N <= 5 uses the N = 5 shape, whose
+// register budget holds the fp32 partials without spilling.
+inline int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false) {
+  if (reduce_scatter && nranks <= 4) return acc32 ? SHAPE_N5 : SHAPE_N2;
+  if (acc32 && nranks <= 5) return SHAPE_N5;
+  if (nranks <= 2) return SHAPE_N2;
+  if (nranks <= 4) return SHAPE_N4;
+  if (nranks == 5) return SHAPE_N5;
+  if (nranks < 12) return SHAPE_W8;
+  return SHAPE_W16;
+}
 
 enum Kind {
   KIND_ALLREDUCE = 0,       // fused: one launch per call
@@ -452,18 +442,40 @@ __global__ void __launch_bounds__(StepShape::kThreads, StepShape::kMinBlocks)
 // ---------------------------------------------------------------------------
 // host-side launch for one dtype (instantiated once per dtype translation unit)
 // ---------------------------------------------------------------------------
-template <int DT, int OP, class SH>
-cudaError_t launch_shaped(int kind, const Args& a, dim3 grid, cudaStream_t s) {
-  const dim3 block(SH::kThreads);
-  constexpr bool kNarrow = DT == DT_F16 || DT == DT_BF16;
-  if (kind == KIND_ALLREDUCE) {
-    if (kNarrow && a.acc32) ar_fused_kernel<DT, OP, kNarrow, SH><<<grid, block, 0, s>>>(a);
-    else ar_fused_kernel<DT, OP, false, SH><<<grid, block, 0, s>>>(a);
-  } else {
-    if (kNarrow && a.acc32) rs_fused_kernel<DT, OP, kNarrow, SH><<<grid, block, 0, s>>>(a);
-    else rs_fused_kernel<DT, OP, false, SH><<<grid, block, 0, s>>>(a);
-  }
+template <int DT, int OP, bool ACC32, class SH>
+cudaError_t launch_ar(const Args& a, dim3 grid, cudaStream_t s) {
+  ar_fused_kernel<DT, OP, ACC32, SH><<<grid, SH::kThreads, 0, s>>>(a);
   return cudaGetLastError();
+}
+template <int DT, int OP, bool ACC32, class SH>
+cudaError_t launch_rs(const Args& a, dim3 grid, cudaStream_t s) {
+  rs_fused_kernel<DT, OP, ACC32, SH><<<grid, SH::kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+template <int DT, int OP, bool ACC32, class SH>
+cudaError_t launch_fused_shape(int kind, const Args& a, dim3 grid, cudaStream_t s) {
+  return kind == KIND_ALLREDUCE ? launch_ar<DT, OP, ACC32, SH>(a, grid, s) : launch_rs<DT, OP, ACC32, SH>(a, grid, s);
+}
+
+// Only the (kind, accumulation, shape) combinations shape_for() can choose are
+// instantiated; any other is refused.
+template <int DT, int OP, bool ACC32>
+cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
+  const bool rs = kind == KIND_REDUCE_SCATTER;
+  switch (a.shape) {
+    case SHAPE_N2:
+      if constexpr (!ACC32) return launch_fused_shape<DT, OP, false, ShapeN2>(kind, a, grid, s);
+      break;
+    case SHAPE_N4:
+      if constexpr (!ACC32) {
+        if (!rs) return launch_ar<DT, OP, false, ShapeN4>(a, grid, s);
+      }
+      break;
+    case SHAPE_N5: return launch_fused_shape<DT, OP, ACC32, ShapeN5>(kind, a, grid, s);
+    case SHAPE_W8: return launch_fused_shape<DT, OP, ACC32, ShapeW8>(kind, a, grid, s);
+    case SHAPE_W16: return launch_fused_shape<DT, OP, ACC32, ShapeW16>(kind, a, grid, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int DT, int OP>
@@ -472,38 +484,23 @@ cudaError_t launch_op(int kind, const Args& a, dim3 grid, cudaStream_t s) {
     ring_rs_step_kernel<DT, OP><<<grid, StepShape::kThreads, 0, s>>>(a);
     return cudaGetLastError();
   }
-  if (a.shape == SHAPE_NARROW) return launch_shaped<DT, OP, NarrowShape>(kind, a, grid, s);
-  return launch_shaped<DT, OP, WideShape>(kind, a, grid, s);
+  constexpr bool kNarrow = DT == DT_F16 || DT == DT_BF16;
+  if (kNarrow && a.acc32) return launch_fused<DT, OP, kNarrow>(kind, a, grid, s);
+  return launch_fused<DT, OP, false>(kind, a, grid, s);
 }
 
-template <int DT>
-cudaError_t launch_dtype(int kind, int op, const Args& a, dim3 grid, cudaStream_t s) {
-  if (kind == KIND_ALLGATHER) {
-    ag_copy_kernel<DT, StepShape><<<grid, StepShape::kThreads, 0, s>>>(a);
-    return cudaGetLastError();
-  }
-  if (kind == KIND_RING_AG_STEP) {
-    ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
-    return cudaGetLastError();
-  }
-  switch (op) {
-    case OP_SUM: return launch_op<DT, OP_SUM>(kind, a, grid, s);
-    case OP_AVG: return launch_op<DT, OP_AVG>(kind, a, grid, s);
-    case OP_MIN: return launch_op<DT, OP_MIN>(kind, a, grid, s);
-    case OP_MAX: return launch_op<DT, OP_MAX>(kind, a, grid, s);
-    case OP_PROD: return launch_op<DT, OP_PROD>(kind, a, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
+template <class SH>
+inline void shape_params_of(int* threads, int* unroll, int* min_blocks) {
+  *threads = SH::kThreads, *unroll = SH::kUnroll, *min_blocks = SH::kMinBlocks;
 }
-
-// Threads, unroll and resident CTAs per SM of a shape, for the host planner.
 inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) {
-  if (shape == SHAPE_WIDE) {
-    *threads = WideShape::kThreads, *unroll = WideShape::kUnroll, *min_blocks = WideShape::kMinBlocks;
-  } else if (shape == SHAPE_NARROW) {
-    *threads = NarrowShape::kThreads, *unroll = NarrowShape::kUnroll, *min_blocks = NarrowShape::kMinBlocks;
-  } else {
-    *threads = StepShape::kThreads, *unroll = StepShape::kUnroll, *min_blocks = StepShape::kMinBlocks;
+  switch (shape) {
+    case SHAPE_N2: return shape_params_of<ShapeN2>(threads, unroll, min_blocks);
+    case SHAPE_N4: return shape_params_of<ShapeN4>(threads, unroll, min_blocks);
+    case SHAPE_N5: return shape_params_of<ShapeN5>(threads, unroll, min_blocks);
+    case SHAPE_W8: return shape_params_of<ShapeW8>(threads, unroll, min_blocks);
+    case SHAPE_W16: return shape_params_of<ShapeW16>(threads, unroll, min_blocks);
+    default: return shape_params_of<StepShape>(threads, unroll, min_blocks);
   }
 }
 

@@ -1,0 +1,52 @@
+// Dispatch to the (dtype, op) slices of ra_launch_op.cu, plus the
+// op-independent kernels (all-gather and the ring's all-gather step).
+#include "ra_kernels.cuh"
+#include "ra_order.cuh"
+
+namespace ra {
+
+#define RA_DECLARE_SLICE(DT, OP)                                                                  \
+  cudaError_t launch_slice_##DT##_##OP(int kind, const Args& a, dim3 grid, cudaStream_t s);       \
+  cudaError_t launch_ordered_slice_##DT##_##OP(bool is_rs, const OrderArgs& o, dim3 grid, cudaStream_t s);
+#define RA_DECLARE_DT(DT) \
+  RA_DECLARE_SLICE(DT, 0) RA_DECLARE_SLICE(DT, 1) RA_DECLARE_SLICE(DT, 2) RA_DECLARE_SLICE(DT, 3) RA_DECLARE_SLICE(DT, 4)
+RA_DECLARE_DT(0)
+RA_DECLARE_DT(1)
+RA_DECLARE_DT(2)
+RA_DECLARE_DT(3)
+
+using SliceFn = cudaError_t (*)(int, const Args&, dim3, cudaStream_t);
+using OrderedSliceFn = cudaError_t (*)(bool, const OrderArgs&, dim3, cudaStream_t);
+#define RA_ROW(DT) {launch_slice_##DT##_0, launch_slice_##DT##_1, launch_slice_##DT##_2, launch_slice_##DT##_3, launch_slice_##DT##_4}
+#define RA_OROW(DT)                                                                              \
+  {launch_ordered_slice_##DT##_0, launch_ordered_slice_##DT##_1, launch_ordered_slice_##DT##_2, \
+   launch_ordered_slice_##DT##_3, launch_ordered_slice_##DT##_4}
+const SliceFn kSlices[4][5] = {RA_ROW(0), RA_ROW(1), RA_ROW(2), RA_ROW(3)};
+const OrderedSliceFn kOrderedSlices[4][5] = {RA_OROW(0), RA_OROW(1), RA_OROW(2), RA_OROW(3)};
+
+template <int DT>
+cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
+  if (kind == KIND_ALLGATHER) ag_copy_kernel<DT, StepShape><<<grid, StepShape::kThreads, 0, s>>>(a);
+  else ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid, cudaStream_t s) {
+  if (dtype < 0 || dtype > 3 || op < 0 || op > 4) return cudaErrorInvalidValue;
+  if (kind == KIND_ALLGATHER || kind == KIND_RING_AG_STEP) {
+    switch (dtype) {
+      case DT_F32: return launch_op_free<DT_F32>(kind, a, grid, s);
+      case DT_F16: return launch_op_free<DT_F16>(kind, a, grid, s);
+      case DT_BF16: return launch_op_free<DT_BF16>(kind, a, grid, s);
+      default: return launch_op_free<DT_I32>(kind, a, grid, s);
+    }
+  }
+  return kSlices[dtype][op](kind, a, grid, s);
+}
+
+cudaError_t launch_ordered_kernel(bool is_rs, int dtype, int op, const OrderArgs& o, dim3 grid, cudaStream_t s) {
+  if (dtype < 0 || dtype > 3 || op < 0 || op > 4) return cudaErrorInvalidValue;
+  return kOrderedSlices[dtype][op](is_rs, o, grid, s);
+}
+
+}  // namespace ra

@@ -123,16 +123,4 @@ cudaError_t launch_ordered_op(bool is_rs, const OrderArgs& o, dim3 grid, cudaStr
   return cudaGetLastError();
 }
 
-template <int DT>
-cudaError_t launch_ordered_dtype(bool is_rs, int op, const OrderArgs& o, dim3 grid, cudaStream_t s) {
-  switch (op) {
-    case OP_SUM: return launch_ordered_op<DT, OP_SUM>(is_rs, o, grid, s);
-    case OP_AVG: return launch_ordered_op<DT, OP_AVG>(is_rs, o, grid, s);
-    case OP_MIN: return launch_ordered_op<DT, OP_MIN>(is_rs, o, grid, s);
-    case OP_MAX: return launch_ordered_op<DT, OP_MAX>(is_rs, o, grid, s);
-    case OP_PROD: return launch_ordered_op<DT, OP_PROD>(is_rs, o, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 }  // namespace ra

@@ -546,8 +546,8 @@ def test_bucketed_allreduce(ra, dtype, op):
     counts = [1000, 3, 77, 4096, 10, 2048, 5, 65536, 1, 333]
     n, length = 5, sum(counts)
     es = ELEM_SIZE[dtype]
-    plan = ra.ra_bucket_plan(counts, 8000 * es, es)
-    assert len(plan) > 3
+    plan = ra.ra_bucket_plan(counts, 3000 * es, es)
+    assert len(plan) == 5
     xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=11)
     sends = [to_device(x, dtype) for x in xs]
     recvs = [torch.zeros_like(s) for s in sends]
