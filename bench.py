@@ -131,10 +131,14 @@ def job_value(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
     return world * bytes_per_rank / (ms_per_step * 1e-3) / GB
 
 
+# the sources that define the fused all-reduce kernel's code
+AR_KERNEL_SOURCES = ("ra_kernels.cuh", "ra_ops.cuh", "ra_plan.h")
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ring_all_reduce_02_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in AR_KERNEL_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]

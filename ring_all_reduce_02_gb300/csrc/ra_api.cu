@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include "../../include/ra.h"
+#include "ra_ag_shape.h"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
 
@@ -118,6 +119,9 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
   return RA_SUCCESS;
 }
 
+// Launch-shape id of the all-gather kernel (its shape lives in ra_ag_shape.h).
+constexpr int kShapeAllGather = 100;
+
 // SMs the launch may fill: all of them, or the caller's budget (max_sms > 0)
 // when other work runs beside the collective.
 ra_status_t sm_budget(int max_sms, int* sms) {
@@ -134,7 +138,11 @@ ra_status_t sm_budget(int max_sms, int* sms) {
 // of the launch shape on the SM budget.
 ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3* grid) {
   int threads, per_thread, min_blocks, sms = 0;
-  ra::shape_params(shape, &threads, &per_thread, &min_blocks);
+  if (shape == kShapeAllGather) {
+    threads = ra::AgShape::kThreads, per_thread = ra::AgShape::kUnroll, min_blocks = ra::AgShape::kMinBlocks;
+  } else {
+    ra::shape_params(shape, &threads, &per_thread, &min_blocks);
+  }
   const ra_status_t st = sm_budget(max_sms, &sms);
   if (st != RA_SUCCESS) return st;
   const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
@@ -248,7 +256,7 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   if (count == 0) return RA_SUCCESS;
   if (order != RA_ORDER_RING) return run_ordered(kind, a, dtype, op, order, max_sms, stream);
   a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
-  a.shape = kind == ra::KIND_ALLGATHER ? ra::SHAPE_STEP
+  a.shape = kind == ra::KIND_ALLGATHER ? kShapeAllGather
                                        : ra::shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0);
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);

@@ -1,5 +1,6 @@
 // Dispatch to the (dtype, op) slices of ra_launch_op.cu, plus the
 // op-independent kernels (all-gather and the ring's all-gather step).
+#include "ra_ag_shape.h"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
 
@@ -26,7 +27,7 @@ const OrderedSliceFn kOrderedSlices[4][5] = {RA_OROW(0), RA_OROW(1), RA_OROW(2),
 
 template <int DT>
 cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
-  if (kind == KIND_ALLGATHER) ag_copy_kernel<DT, StepShape><<<grid, StepShape::kThreads, 0, s>>>(a);
+  if (kind == KIND_ALLGATHER) ag_copy_kernel<DT, AgShape><<<grid, AgShape::kThreads, 0, s>>>(a);
   else ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
