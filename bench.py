@@ -507,33 +507,36 @@ def run_overlap(args):
             compute()
         main.wait_stream(cs)
 
-    def comm_only(max_sms):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def comm_only(max_sms, engine):
         ms.wait_stream(main)
-        ra.ra_allreduce_buckets(sends, recvs, plan, op, max_sms=max_sms, stream=ms)
+        ra.ra_allreduce_buckets(sends, recvs, plan, op, max_sms=max_sms, engine=engine, status=status, stream=ms)
         main.wait_stream(ms)
 
-    def overlapped(max_sms):
+    def overlapped(max_sms, engine):
         events = [torch.cuda.Event() for _ in plan]
         cs.wait_stream(main)
         ms.wait_stream(main)
         with torch.cuda.stream(cs):
             compute(events)
-        ra.ra_allreduce_buckets(sends, recvs, plan, op, ready_events=events, max_sms=max_sms, stream=ms)
+        ra.ra_allreduce_buckets(sends, recvs, plan, op, ready_events=events, max_sms=max_sms, engine=engine,
+                                status=status, stream=ms)
         main.wait_stream(cs)
         main.wait_stream(ms)
 
     c_ms = timed(compute_only)
     flops = sum(2 * c * tokens for _, c in plan)
     s_bytes = length * 2
-    for max_sms in (0, 76, 38, 16, 8):
-        a_ms = timed(lambda: comm_only(max_sms))
-        t_ms = timed(lambda: overlapped(max_sms))
+    for engine, max_sms in [("registers", m) for m in (0, 76, 38, 16, 8)] + [("bulk", m) for m in (0, 76, 38, 16, 8)]:
+        a_ms = timed(lambda: comm_only(max_sms, engine))
+        t_ms = timed(lambda: overlapped(max_sms, engine))
         rec = {"mode": "overlap", "workload": "ar_n8_bf16_avg_gpt2m", "buckets": len(plan),
-               "bucket_cap_bytes": 25 * 1000 * 1000, "tokens": tokens, "max_sms": max_sms,
+               "bucket_cap_bytes": 25 * 1000 * 1000, "tokens": tokens, "engine": engine, "max_sms": max_sms,
                "compute_ms": round(c_ms, 3), "compute_tflops": round(flops / (c_ms * 1e-3) / 1e12, 1),
                "allreduce_ms": round(a_ms, 3), "allreduce_algbw_GBps": round(s_bytes / (a_ms * 1e-3) / GB, 1),
                "overlapped_ms": round(t_ms, 3), "exposed_comm_ms": round(t_ms - c_ms, 3),
-               "hidden_fraction": round((c_ms + a_ms - t_ms) / a_ms, 3)}
+               "hidden_fraction": round((c_ms + a_ms - t_ms) / a_ms, 3), "status": int(status.item())}
         print(json.dumps(rec), flush=True)
     return 0
 

@@ -128,22 +128,39 @@ typedef enum {
                          No effect on fp32 and int32 buffers. */
 } ra_accum_t;
 
+/* How the fused all-reduce moves its loads. */
+typedef enum {
+  RA_ENGINE_REGISTERS = 0, /* every thread keeps its loads in flight in registers (the default) */
+  RA_ENGINE_BULK = 1       /* a producer thread per CTA streams tiles of all ranks into shared memory
+                              with bulk copies (the Tensor Memory Accelerator) and the other warps fold
+                              from there: several times the bytes in flight per SM, for runs confined
+                              to a few SMs by max_sms. All-reduce with the ring order and dtype
+                              accumulation, nranks <= 16; needs `status` */
+} ra_engine_t;
+
 /* Options of the extended calls; NULL means all defaults. */
 typedef struct {
-  ra_order_t order; /* RA_ORDER_RING by default */
-  ra_accum_t accum; /* RA_ACCUM_DTYPE by default */
-  int max_sms;      /* 0: the launch may fill every SM; k > 0: at most k SMs' worth of CTAs, leaving the
-                       rest to work running beside the collective (arjunsriva.com "AllReduce, All the Way
-                       Down": communication kernels compete with compute for SMs) */
+  ra_order_t order;   /* RA_ORDER_RING by default */
+  ra_accum_t accum;   /* RA_ACCUM_DTYPE by default */
+  int max_sms;        /* 0: the launch may fill every SM; k > 0: at most k SMs' worth of CTAs, leaving the
+                         rest to work running beside the collective (arjunsriva.com "AllReduce, All the
+                         Way Down": communication kernels compete with compute for SMs) */
+  ra_engine_t engine; /* RA_ENGINE_REGISTERS by default */
+  int* status;        /* RA_ENGINE_BULK only: one int of device memory, owned by the caller, that the
+                         kernel sets to a nonzero code if one of its bounded waits gives up (1: a
+                         bulk copy did not land within 1 s; 2: a stage was not released within 1 s)
+                         instead of hanging; it is never cleared by the library */
 } ra_options_t;
 
 /*
  * All-reduce / reduce-scatter with options: ra_allreduce(...) is
  * ra_allreduce_ex(..., NULL, stream). Same buffers, in-place rules and errors
  * as the plain calls, plus RA_ERR_UNSUPPORTED for RA_ORDER_RABENSEIFNER with a
- * nranks that is not a power of two and for RA_ACCUM_FP32 with an order other
- * than the ring, and RA_ERR_INVALID_ARG for an unknown order/accum or a
- * negative max_sms.
+ * nranks that is not a power of two, for RA_ACCUM_FP32 with an order other
+ * than the ring, and for RA_ENGINE_BULK outside its range (reduce-scatter,
+ * another order or accumulation, nranks > 16, buffers without a common
+ * address phase), and RA_ERR_INVALID_ARG for an unknown order/accum/engine,
+ * a negative max_sms or RA_ENGINE_BULK without a status word.
  */
 ra_status_t ra_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, size_t count, ra_dtype_t dtype,
                             ra_op_t op, int nranks, const ra_options_t* options, void* stream);
@@ -207,13 +224,15 @@ ra_status_t ra_chunk_range(size_t count, int nranks, int c, size_t* begin, size_
 
 /*
  * Planner introspection (host only, no GPU): how chunk c is split between the
- * 16-byte vector path and the per-element path for buffers whose common
- * address phase (address mod 16) is `phase_bytes` and whose elements are
- * `elem_size` bytes. Writes [vec_begin, vec_end) (elements handled as 16-byte
- * vectors; empty if vec_begin == vec_end) inside [begin, end); the elements of
- * the chunk outside it take the per-element path.
+ * vector path and the per-element path for buffers of `elem_size`-byte
+ * elements that share their address phase `phase_bytes` modulo `align_bytes`
+ * (a power of two from ra_vector_bytes() to 512; the library uses the largest
+ * such alignment the buffers share). Writes [vec_begin, vec_end) (elements
+ * moved as whole vectors, starting on the alignment grid; empty if vec_begin
+ * == vec_end) inside [begin, end); the rest of the chunk takes the
+ * per-element path.
  */
-ra_status_t ra_plan_chunk(size_t count, int nranks, int c, int elem_size, int phase_bytes,
+ra_status_t ra_plan_chunk(size_t count, int nranks, int c, int elem_size, int align_bytes, int phase_bytes,
                           size_t* begin, size_t* end, size_t* vec_begin, size_t* vec_end);
 
 /* A static, human-readable name for a status code. */
@@ -221,6 +240,18 @@ const char* ra_status_string(ra_status_t status);
 
 /* The cudaError_t of the last RA_ERR_CUDA returned on the calling thread (0 if none). */
 int ra_last_cuda_error(void);
+
+/*
+ * Self-test of the bulk engine's bounded waits (host-visible failure
+ * reporting without a GPU fault): runs the RA_ENGINE_BULK all-reduce with the
+ * first tile of CTA (0, 0) never copied in, so that CTA's consumers wait for
+ * it in vain, give up after 1 s, write a nonzero code to *status (device int,
+ * caller-owned, which should be 0 before the call) and wind the kernel down;
+ * the launch completes and the context stays usable. The receive buffers'
+ * contents are unspecified afterwards. Same arguments as ra_allreduce.
+ */
+ra_status_t ra_selftest_bulk_timeout(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                     ra_dtype_t dtype, ra_op_t op, int nranks, int* status, void* stream);
 
 /* Bytes per vector access of this build's kernels (16 or 32): the address
  * phase (address mod this) the buffers must share for the vector path. */

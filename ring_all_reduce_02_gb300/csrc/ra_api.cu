@@ -8,12 +8,14 @@
 
 #include "../../include/ra.h"
 #include "ra_ag_shape.h"
+#include "ra_bulk.cuh"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
 
 namespace ra {
 cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_ordered_kernel(bool is_rs, int dtype, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
+cudaError_t launch_bulk_kernel(int dtype, int op, const BulkArgs& b, dim3 grid, size_t smem, cudaStream_t s);
 }  // namespace ra
 
 namespace {
@@ -87,13 +89,23 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
 
   // Address phases: the N-way side must share one phase for the vector path
   // (AR: all sources and destinations; RS: the sources; AG: the destinations).
+  // The grid is laid on the largest alignment, up to 512 bytes (one warp's
+  // 16-byte accesses), at which every such buffer shares its phase.
   const Range* wide = kind == ra::KIND_ALLGATHER ? recv : send;
-  const unsigned phase = (unsigned)(wide[0].lo % ra::kVecBytes);
-  bool same = true;
-  for (int r = 0; r < nranks; ++r) {
-    same = same && (wide[r].lo % ra::kVecBytes) == phase;
-    if (kind == ra::KIND_ALLREDUCE) same = same && (recv[r].lo % ra::kVecBytes) == phase;
+  unsigned align = ra::kLineAlignMax;
+  for (; align >= (unsigned)ra::kVecBytes; align /= 2) {
+    const unsigned ph = (unsigned)(wide[0].lo % align);
+    bool same_here = true;
+    for (int r = 0; r < nranks; ++r) {
+      same_here = same_here && (wide[r].lo % align) == ph;
+      if (kind == ra::KIND_ALLREDUCE) same_here = same_here && (recv[r].lo % align) == ph;
+    }
+    if (same_here) break;
   }
+  const bool same = align >= (unsigned)ra::kVecBytes;
+  if (!same) align = ra::kVecBytes;
+  const unsigned phase_a = (unsigned)(wide[0].lo % align);
+  const unsigned phase = (unsigned)(wide[0].lo % ra::kVecBytes);
   uint64_t compact_aligned = 0;
   if (kind != ra::KIND_ALLREDUCE) {
     const Range* compact = kind == ra::KIND_ALLGATHER ? send : recv;
@@ -110,7 +122,8 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
   a->count = count;
   a->compact_aligned = compact_aligned;
   a->nranks = nranks;
-  a->head = (int)(((ra::kVecBytes - phase) % ra::kVecBytes) / (unsigned)es);
+  a->head = (int)(((align - phase_a) % align) / (unsigned)es);
+  a->align_elems = (int)(align / (unsigned)es);
   a->vec_ok = same ? 1 : 0;
   a->inv_n = 1.0f / (float)nranks;
   a->step = 0;
@@ -163,7 +176,38 @@ ra_status_t launch(int kind, int dtype, int op, const ra::Args& a, dim3 grid, vo
   return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
 }
 
-const ra_options_t kDefaultOptions = {RA_ORDER_RING, RA_ACCUM_DTYPE, 0};
+const ra_options_t kDefaultOptions = {RA_ORDER_RING, RA_ACCUM_DTYPE, 0, RA_ENGINE_REGISTERS, nullptr};
+
+// The bulk engine: tiles of tile_vecs vectors per rank, as many stages as fit
+// in about 200 KB of shared memory (2..8), one CTA per SM on the budget.
+constexpr size_t kBulkSmemBudget = 200 * 1024;
+
+ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* status, void* stream,
+                     int withhold_first = 0) {
+  ra::BulkArgs b;
+  b.base = a;
+  b.status = status;
+  b.withhold_first = withhold_first;
+  const int n = a.nranks;
+  b.tile_vecs = n <= 8 ? 256 : 128;  // 4 KB or 2 KB per rank per stage (16-byte vectors)
+  const size_t stage_bytes = (size_t)n * b.tile_vecs * ra::kVecBytes;
+  size_t stages = kBulkSmemBudget / stage_bytes;
+  if (stages > 8) stages = 8;
+  if (stages < 2) return RA_ERR_UNSUPPORTED;
+  b.stages = (uint32_t)stages;
+  const size_t smem = 128 * ((2 * stages * 8 + 127) / 128) + stages * stage_bytes;
+  int sms = 0;
+  const ra_status_t st = sm_budget(max_sms, &sms);
+  if (st != RA_SUCCESS) return st;
+  const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
+  const uint64_t tiles = ((a.count + n - 1) / n / v) / b.tile_vecs + 1;
+  uint64_t gx = (uint64_t)sms / (uint64_t)n;
+  if (gx > tiles) gx = tiles;
+  if (gx < 1) gx = 1;
+  const cudaError_t err = ra::launch_bulk_kernel(dtype, op, b, dim3((unsigned)gx, (unsigned)n), smem,
+                                                 static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
+}
 
 // ---- reduction programs of the other orders --------------------------------
 // A program is a list of steps slot[a] = op(slot[a], slot[b]) over the N rank
@@ -247,13 +291,23 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   if (kind == ra::KIND_ALLGATHER) op = RA_SUM;  // no reduction; any valid op is accepted
   if (options == nullptr) options = &kDefaultOptions;
   const int order = options->order, accum = options->accum, max_sms = options->max_sms;
+  const int engine = options->engine;
   if (accum != RA_ACCUM_DTYPE && accum != RA_ACCUM_FP32) return RA_ERR_INVALID_ARG;
   if (order < RA_ORDER_RING || order > RA_ORDER_RABENSEIFNER || max_sms < 0) return RA_ERR_INVALID_ARG;
+  if (engine != RA_ENGINE_REGISTERS && engine != RA_ENGINE_BULK) return RA_ERR_INVALID_ARG;
+  if (engine == RA_ENGINE_BULK && options->status == nullptr) return RA_ERR_INVALID_ARG;
   ra_status_t st = prepare(kind, sendbufs, recvbufs, count, dtype, op, nranks, &a);
   if (st != RA_SUCCESS) return st;
   if (order == RA_ORDER_RABENSEIFNER && (nranks & (nranks - 1))) return RA_ERR_UNSUPPORTED;
   if (order != RA_ORDER_RING && accum == RA_ACCUM_FP32) return RA_ERR_UNSUPPORTED;
+  if (engine == RA_ENGINE_BULK &&
+      (kind != ra::KIND_ALLREDUCE || order != RA_ORDER_RING || accum != RA_ACCUM_DTYPE || nranks > 16))
+    return RA_ERR_UNSUPPORTED;
   if (count == 0) return RA_SUCCESS;
+  if (engine == RA_ENGINE_BULK) {
+    if (!a.vec_ok) return RA_ERR_UNSUPPORTED;
+    return run_bulk(a, dtype, op, max_sms, options->status, stream);
+  }
   if (order != RA_ORDER_RING) return run_ordered(kind, a, dtype, op, order, max_sms, stream);
   a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
   a.shape = kind == ra::KIND_ALLGATHER ? kShapeAllGather
@@ -431,16 +485,19 @@ ra_status_t ra_chunk_range(size_t count, int nranks, int c, size_t* begin, size_
   return RA_SUCCESS;
 }
 
-ra_status_t ra_plan_chunk(size_t count, int nranks, int c, int elem_size_bytes, int phase_bytes,
+ra_status_t ra_plan_chunk(size_t count, int nranks, int c, int elem_size_bytes, int align_bytes, int phase_bytes,
                           size_t* begin, size_t* end, size_t* vec_begin, size_t* vec_end) {
   if (elem_size_bytes != 2 && elem_size_bytes != 4) return RA_ERR_INVALID_ARG;
-  if (phase_bytes < 0 || phase_bytes >= ra::kVecBytes || phase_bytes % elem_size_bytes) return RA_ERR_INVALID_ARG;
+  if (align_bytes < ra::kVecBytes || align_bytes > ra::kLineAlignMax || (align_bytes & (align_bytes - 1)))
+    return RA_ERR_INVALID_ARG;
+  if (phase_bytes < 0 || phase_bytes >= align_bytes || phase_bytes % elem_size_bytes) return RA_ERR_INVALID_ARG;
   if (vec_begin == nullptr || vec_end == nullptr) return RA_ERR_INVALID_ARG;
   const ra_status_t st = ra_chunk_range(count, nranks, c, begin, end);
   if (st != RA_SUCCESS) return st;
-  const uint64_t head = (uint64_t)((ra::kVecBytes - phase_bytes) % ra::kVecBytes) / elem_size_bytes;
+  const uint64_t head = (uint64_t)((align_bytes - phase_bytes) % align_bytes) / elem_size_bytes;
   uint64_t vb, ve;
-  ra::vec_range(*begin, *end, head, (uint64_t)(ra::kVecBytes / elem_size_bytes), &vb, &ve);
+  ra::vec_range(*begin, *end, head, (uint64_t)(align_bytes / elem_size_bytes),
+                (uint64_t)(ra::kVecBytes / elem_size_bytes), &vb, &ve);
   *vec_begin = (size_t)vb;
   *vec_end = (size_t)ve;
   return RA_SUCCESS;
@@ -460,5 +517,15 @@ const char* ra_status_string(ra_status_t status) {
 int ra_last_cuda_error(void) { return g_last_cuda_error; }
 
 int ra_vector_bytes(void) { return ra::kVecBytes; }
+
+ra_status_t ra_selftest_bulk_timeout(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                     ra_dtype_t dtype, ra_op_t op, int nranks, int* status, void* stream) {
+  if (status == nullptr) return RA_ERR_INVALID_ARG;
+  ra::Args a;
+  const ra_status_t st = prepare(ra::KIND_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, nranks, &a);
+  if (st != RA_SUCCESS) return st;
+  if (nranks > 16 || !a.vec_ok || count == 0) return RA_ERR_UNSUPPORTED;
+  return run_bulk(a, dtype, op, 0, status, stream, /*withhold_first=*/1);
+}
 
 }  // extern "C"

@@ -54,11 +54,19 @@ struct Shape {
   static constexpr int kUnroll = UNROLL;         // vectors per thread per trip
   static constexpr int kBatch = BATCH;           // ranks whose loads are in flight together
 };
+#ifndef RA_TUNE_SHAPE
 using ShapeN2 = Shape<128, 8, 2, 4>;    // nranks 1..2
 using ShapeN4 = Shape<256, 1, 8, 4>;    // nranks 3..4
 using ShapeN5 = Shape<256, 2, 2, 4>;    // nranks 5
 using ShapeW8 = Shape<256, 1, 4, 8>;    // nranks 6..11
 using ShapeW16 = Shape<256, 1, 4, 4>;   // nranks 12..64
+#else  // tuning sweeps: one shape (RA_TUNE_T, _MB, _U, _B) for every rank count
+using ShapeN2 = Shape<RA_TUNE_T, RA_TUNE_MB, RA_TUNE_U, RA_TUNE_B>;
+using ShapeN4 = ShapeN2;
+using ShapeN5 = ShapeN2;
+using ShapeW8 = ShapeN2;
+using ShapeW16 = ShapeN2;
+#endif
 using StepShape = Shape<256, 2, 1, 1>;  // ring-step and all-gather kernels
 enum ShapeId { SHAPE_N2 = 0, SHAPE_N4 = 1, SHAPE_N5 = 2, SHAPE_W8 = 3, SHAPE_W16 = 4, SHAPE_STEP = 5 };
 
@@ -91,7 +99,8 @@ struct Args {
   uint64_t count;            // elements per rank (the full vector length L)
   uint64_t compact_aligned;  // bit c: the compact buffer of chunk c shares the vector phase
   int nranks;
-  int head;    // first element index on the common vector grid, in [0, V)
+  int head;        // first element index whose address is on the common line-aligned grid
+  int align_elems; // elements per line-alignment step (a multiple of V)
   int vec_ok;  // the N-way side (AR/RS: sources and AR destinations; AG: destinations) shares one phase
   float inv_n; // 1.0f / nranks, rounded in fp32
   int step;    // ring step of a KIND_RING_* launch
@@ -253,7 +262,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(
   const int n = a.nranks, c = blockIdx.y;
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
-  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
   const Span sp = cta_span<SH>((ve - vb) / V);
   for (uint64_t j0 = sp.jbeg + threadIdx.x; j0 < sp.jend; j0 += sp.jstride) {
     uint64_t off[kUnroll];
@@ -290,7 +299,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
   const int n = a.nranks, c = blockIdx.y;
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
-  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
   const Span sp = cta_span<SH>((ve - vb) / V);
   void* out = a.dst[c];
   const bool out_vec = (a.compact_aligned >> c) & 1u;
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ag_copy_kernel(c
   const int n = a.nranks, c = blockIdx.y;
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
-  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
   const Span sp = cta_span<SH>((ve - vb) / V);
   const void* in = a.src[c];
   const bool in_vec = (a.compact_aligned >> c) & 1u;
@@ -402,7 +411,7 @@ __global__ void __launch_bounds__(StepShape::kThreads, StepShape::kMinBlocks)
   const bool finish = (OP == OP_AVG) && (s == n - 2);
   const uint64_t b0 = chunk_begin(cc, n, a.count), b1 = chunk_begin(cc + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
-  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
   const uint64_t nv = (ve - vb) / V;
   for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < nv; j += (uint64_t)gridDim.x * kThreads) {
     const uint64_t off = (vb + j * V) * ES;
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(StepShape::kThreads, StepShape::kMinBlocks)
   void* out = a.dst[r];
   const uint64_t b0 = chunk_begin(cc, n, a.count), b1 = chunk_begin(cc + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
-  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
   const uint64_t nv = (ve - vb) / V;
   for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < nv; j += (uint64_t)gridDim.x * kThreads) {
     const uint64_t off = (vb + j * V) * ES;

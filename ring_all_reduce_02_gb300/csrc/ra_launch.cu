@@ -1,6 +1,7 @@
 // Dispatch to the (dtype, op) slices of ra_launch_op.cu, plus the
 // op-independent kernels (all-gather and the ring's all-gather step).
 #include "ra_ag_shape.h"
+#include "ra_bulk.cuh"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
 
@@ -8,7 +9,8 @@ namespace ra {
 
 #define RA_DECLARE_SLICE(DT, OP)                                                                  \
   cudaError_t launch_slice_##DT##_##OP(int kind, const Args& a, dim3 grid, cudaStream_t s);       \
-  cudaError_t launch_ordered_slice_##DT##_##OP(bool is_rs, const OrderArgs& o, dim3 grid, cudaStream_t s);
+  cudaError_t launch_ordered_slice_##DT##_##OP(bool is_rs, const OrderArgs& o, dim3 grid, cudaStream_t s); \
+  cudaError_t launch_bulk_slice_##DT##_##OP(const BulkArgs& b, dim3 grid, size_t smem, cudaStream_t s);
 #define RA_DECLARE_DT(DT) \
   RA_DECLARE_SLICE(DT, 0) RA_DECLARE_SLICE(DT, 1) RA_DECLARE_SLICE(DT, 2) RA_DECLARE_SLICE(DT, 3) RA_DECLARE_SLICE(DT, 4)
 RA_DECLARE_DT(0)
@@ -22,8 +24,13 @@ using OrderedSliceFn = cudaError_t (*)(bool, const OrderArgs&, dim3, cudaStream_
 #define RA_OROW(DT)                                                                              \
   {launch_ordered_slice_##DT##_0, launch_ordered_slice_##DT##_1, launch_ordered_slice_##DT##_2, \
    launch_ordered_slice_##DT##_3, launch_ordered_slice_##DT##_4}
+#define RA_BROW(DT)                                                                         \
+  {launch_bulk_slice_##DT##_0, launch_bulk_slice_##DT##_1, launch_bulk_slice_##DT##_2, \
+   launch_bulk_slice_##DT##_3, launch_bulk_slice_##DT##_4}
+using BulkSliceFn = cudaError_t (*)(const BulkArgs&, dim3, size_t, cudaStream_t);
 const SliceFn kSlices[4][5] = {RA_ROW(0), RA_ROW(1), RA_ROW(2), RA_ROW(3)};
 const OrderedSliceFn kOrderedSlices[4][5] = {RA_OROW(0), RA_OROW(1), RA_OROW(2), RA_OROW(3)};
+const BulkSliceFn kBulkSlices[4][5] = {RA_BROW(0), RA_BROW(1), RA_BROW(2), RA_BROW(3)};
 
 template <int DT>
 cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
@@ -48,6 +55,11 @@ cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid,
 cudaError_t launch_ordered_kernel(bool is_rs, int dtype, int op, const OrderArgs& o, dim3 grid, cudaStream_t s) {
   if (dtype < 0 || dtype > 3 || op < 0 || op > 4) return cudaErrorInvalidValue;
   return kOrderedSlices[dtype][op](is_rs, o, grid, s);
+}
+
+cudaError_t launch_bulk_kernel(int dtype, int op, const BulkArgs& b, dim3 grid, size_t smem, cudaStream_t s) {
+  if (dtype < 0 || dtype > 3 || op < 0 || op > 4) return cudaErrorInvalidValue;
+  return kBulkSlices[dtype][op](b, grid, smem, s);
 }
 
 }  // namespace ra

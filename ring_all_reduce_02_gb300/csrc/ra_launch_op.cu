@@ -1,6 +1,7 @@
 // One (dtype, op) slice of the kernel instantiations. The build compiles this
 // file once per pair, with RA_SLICE_DT and RA_SLICE_OP set, so the twenty
 // slices compile in parallel; ra_launch.cu dispatches to them.
+#include "ra_bulk.cuh"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
 
@@ -18,5 +19,9 @@ cudaError_t RA_CAT3(launch_slice, RA_SLICE_DT, RA_SLICE_OP)(int kind, const Args
 cudaError_t RA_CAT3(launch_ordered_slice, RA_SLICE_DT, RA_SLICE_OP)(bool is_rs, const OrderArgs& o, dim3 grid,
                                                                     cudaStream_t s) {
   return launch_ordered_op<RA_SLICE_DT, RA_SLICE_OP>(is_rs, o, grid, s);
+}
+cudaError_t RA_CAT3(launch_bulk_slice, RA_SLICE_DT, RA_SLICE_OP)(const BulkArgs& b, dim3 grid, size_t smem,
+                                                                 cudaStream_t s) {
+  return launch_bulk_op<RA_SLICE_DT, RA_SLICE_OP>(b, grid, smem, s);
 }
 }  // namespace ra

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kOrdThreads) ordered_kernel(const __grid_const
   const int pr = (int)((o.chunk_prog >> c) & 1u);
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
-  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, V, &vb, &ve);
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
   const uint64_t nv = (ve - vb) / V;
   Vec* my = reinterpret_cast<Vec*>(slots) + threadIdx.x;  // slot r at my[r * kOrdThreads]
   void* out = a.dst[c];

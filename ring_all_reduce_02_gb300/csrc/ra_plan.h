@@ -8,8 +8,9 @@
 // Within a chunk, elements whose byte address lies on the common kVecBytes grid
 // of all buffers are moved as whole vectors: the grid is {head + k*V}, with
 // V = kVecBytes / elem_size and head the first element index whose address is
-// kVecBytes-aligned. A chunk's vector part is the largest run of whole vectors inside it;
-// the at most 2(V-1) elements at its two ends take the per-element path.
+// aligned to the common line alignment (16..512 bytes, see vec_range). A chunk's
+// vector part runs from the first line-aligned element to its last whole vector;
+// the elements before and after it take the per-element path.
 #pragma once
 
 #include <stdint.h>
@@ -33,17 +34,25 @@ RA_HD uint64_t chunk_begin(int c, int n, uint64_t count) {
   return ((uint64_t)c * count) / (uint64_t)n;
 }
 
-// [vb, ve): whole vectors of the grid {head + k*V} inside [b0, b1).
-// vb == ve when the chunk holds no whole vector.
-RA_HD void vec_range(uint64_t b0, uint64_t b1, uint64_t head, uint64_t v, uint64_t* vb,
+// [vb, ve): whole vectors of the chunk [b0, b1), starting at the first element
+// of the alignment grid {head + k*align} at or after b0 (align is a multiple of
+// v, so the start is also on the vector grid) and ending at the last whole
+// vector. Starting on a line-aligned boundary keeps every warp's contiguous
+// access inside whole cache lines and DRAM sectors. vb == ve (== b0) when no
+// whole vector fits.
+RA_HD void vec_range(uint64_t b0, uint64_t b1, uint64_t head, uint64_t align, uint64_t v, uint64_t* vb,
                      uint64_t* ve) {
-  const uint64_t lo = b0 <= head ? head : head + ((b0 - head + v - 1) / v) * v;
+  const uint64_t lo = b0 <= head ? head : head + ((b0 - head + align - 1) / align) * align;
   if (b1 < lo + v) {
     *vb = *ve = b0;
     return;
   }
   *vb = lo;
-  *ve = head + ((b1 - head) / v) * v;
+  *ve = lo + ((b1 - lo) / v) * v;
 }
+
+// Largest alignment (bytes) the vector grid is laid on: every buffer's address
+// shares its phase modulo this.
+constexpr int kLineAlignMax = 512;
 
 }  // namespace ra

@@ -26,17 +26,22 @@ RA_MAX_RANKS = 64
 # every symbol include/ra.h declares
 EXPORTS = ("ra_allreduce", "ra_reduce_scatter", "ra_allgather", "ra_allreduce_ex", "ra_reduce_scatter_ex",
            "ra_bucket_plan", "ra_allreduce_buckets", "ra_allreduce_ringsteps", "ra_chunk_range", "ra_plan_chunk",
-           "ra_status_string", "ra_last_cuda_error", "ra_vector_bytes")
+           "ra_status_string", "ra_last_cuda_error", "ra_vector_bytes", "ra_selftest_bulk_timeout")
+ENGINE_CODES = {"registers": 0, "bulk": 1}
 
 
 class Options(ctypes.Structure):
     """ra_options_t."""
 
-    _fields_ = [("order", ctypes.c_int), ("accum", ctypes.c_int), ("max_sms", ctypes.c_int)]
+    _fields_ = [("order", ctypes.c_int), ("accum", ctypes.c_int), ("max_sms", ctypes.c_int),
+                ("engine", ctypes.c_int), ("status", ctypes.c_void_p)]
 
 
-def options(order: str = "ring", accum: str = "dtype", max_sms: int = 0) -> Options:
-    return Options(ORDER_CODES[order], ACCUM_CODES[accum], max_sms)
+def options(order: str = "ring", accum: str = "dtype", max_sms: int = 0, engine: str = "registers",
+            status=None) -> Options:
+    """ra_options_t; ``status`` is a device int32 tensor (or address) for the bulk engine."""
+    st = status.data_ptr() if hasattr(status, "data_ptr") else status
+    return Options(ORDER_CODES[order], ACCUM_CODES[accum], max_sms, ENGINE_CODES[engine], st or None)
 
 
 class RaError(RuntimeError):
@@ -80,7 +85,7 @@ def lib() -> ctypes.CDLL:
             L.ra_allreduce_ringsteps.restype = I
             L.ra_chunk_range.argtypes = [SZ, I, I, PSZ, PSZ]
             L.ra_chunk_range.restype = I
-            L.ra_plan_chunk.argtypes = [SZ, I, I, I, I, PSZ, PSZ, PSZ, PSZ]
+            L.ra_plan_chunk.argtypes = [SZ, I, I, I, I, I, PSZ, PSZ, PSZ, PSZ]
             L.ra_plan_chunk.restype = I
             L.ra_status_string.argtypes = [I]
             L.ra_status_string.restype = ctypes.c_char_p
@@ -88,6 +93,8 @@ def lib() -> ctypes.CDLL:
             L.ra_last_cuda_error.restype = I
             L.ra_vector_bytes.argtypes = []
             L.ra_vector_bytes.restype = I
+            L.ra_selftest_bulk_timeout.argtypes = [PP, PP, SZ, I, I, I, VP, VP]
+            L.ra_selftest_bulk_timeout.restype = I
             _lib = L
     return _lib
 
@@ -143,10 +150,10 @@ def call(name: str, send_ptrs, recv_ptrs, count: int, dtype: int, op: int, nrank
 
 
 def call_ex(name: str, send_ptrs, recv_ptrs, count: int, dtype: int, op: int, nranks: int, order: int,
-            accum: int, stream: int, max_sms: int = 0) -> int:
+            accum: int, stream: int, max_sms: int = 0, engine: int = 0, status: int = 0) -> int:
     """Raw C call of ra_allreduce_ex / ra_reduce_scatter_ex; returns the ra_status_t."""
     f = getattr(lib(), name)
-    opts = Options(order, accum, max_sms)
+    opts = Options(order, accum, max_sms, engine, status or None)
     return f(ptr_array(send_ptrs), ptr_array(recv_ptrs), count, dtype, op, nranks, ctypes.byref(opts),
              ctypes.c_void_p(stream or None))
 
@@ -161,13 +168,14 @@ def ra_allreduce(sendbufs, recvbufs, op: str = "sum", stream=None) -> None:
 
 
 def ra_allreduce_ex(sendbufs, recvbufs, op: str = "sum", order: str = "ring", accum: str = "dtype",
-                    max_sms: int = 0, stream=None) -> None:
-    """All-reduce with a reduction order (ring | tree | rabenseifner), accumulation (dtype | fp32)
-    and an SM budget (0 = all SMs)."""
+                    max_sms: int = 0, engine: str = "registers", status=None, stream=None) -> None:
+    """All-reduce with a reduction order (ring | tree | rabenseifner), accumulation (dtype | fp32),
+    an SM budget (0 = all SMs) and an engine (registers | bulk; bulk needs a device int32 ``status``)."""
     count = _check_full(sendbufs, recvbufs, "ra_allreduce_ex")
+    st_ptr = status.data_ptr() if status is not None else 0
     st = call_ex("ra_allreduce_ex", [t.data_ptr() for t in sendbufs], [t.data_ptr() for t in recvbufs], count,
                  dtype_code(sendbufs[0]), OP_CODES[op], len(sendbufs), ORDER_CODES[order], ACCUM_CODES[accum],
-                 _stream_ptr(stream), max_sms)
+                 _stream_ptr(stream), max_sms, ENGINE_CODES[engine], st_ptr)
     if st:
         raise RaError(st, "ra_allreduce_ex")
 
@@ -242,7 +250,8 @@ def ra_bucket_plan(param_counts, bucket_bytes: int, elem_size: int):
 
 
 def ra_allreduce_buckets(sendbufs, recvbufs, buckets, op: str = "sum", ready_events=None, order: str = "ring",
-                         accum: str = "dtype", max_sms: int = 0, stream=None) -> None:
+                         accum: str = "dtype", max_sms: int = 0, engine: str = "registers", status=None,
+                         stream=None) -> None:
     """All-reduce every bucket (begin, count) of the flat buffers, each after its ready event."""
     count = _check_full(sendbufs, recvbufs, "ra_allreduce_buckets")
     m = len(buckets)
@@ -251,7 +260,7 @@ def ra_allreduce_buckets(sendbufs, recvbufs, buckets, op: str = "sum", ready_eve
     events = None
     if ready_events is not None:
         events = ptr_array([int(e.cuda_event) if e is not None else 0 for e in ready_events])
-    opts = options(order, accum, max_sms)
+    opts = options(order, accum, max_sms, engine, status)
     st = lib().ra_allreduce_buckets(ptr_array([t.data_ptr() for t in sendbufs]),
                                     ptr_array([t.data_ptr() for t in recvbufs]), count, dtype_code(sendbufs[0]),
                                     OP_CODES[op], len(sendbufs), m, begin, cnt, events, ctypes.byref(opts),
@@ -268,10 +277,10 @@ def ra_chunk_range(count: int, nranks: int, c: int) -> tuple[int, int]:
     return b.value, e.value
 
 
-def ra_plan_chunk(count: int, nranks: int, c: int, elem_size: int, phase_bytes: int):
+def ra_plan_chunk(count: int, nranks: int, c: int, elem_size: int, phase_bytes: int, align_bytes: int = 16):
     """(begin, end, vec_begin, vec_end) of chunk c: which part takes the vector path."""
     out = [ctypes.c_size_t() for _ in range(4)]
-    st = lib().ra_plan_chunk(count, nranks, c, elem_size, phase_bytes, *[ctypes.byref(o) for o in out])
+    st = lib().ra_plan_chunk(count, nranks, c, elem_size, align_bytes, phase_bytes, *[ctypes.byref(o) for o in out])
     if st:
         raise RaError(st, "ra_plan_chunk")
     return tuple(o.value for o in out)
@@ -279,6 +288,17 @@ def ra_plan_chunk(count: int, nranks: int, c: int, elem_size: int, phase_bytes: 
 
 def ra_status_string(status: int) -> str:
     return lib().ra_status_string(status).decode()
+
+
+def ra_selftest_bulk_timeout(sendbufs, recvbufs, status, op: str = "sum", stream=None) -> None:
+    """Run the bulk engine with one tile withheld: its bounded wait must give up and set ``status``."""
+    count = _check_full(sendbufs, recvbufs, "ra_selftest_bulk_timeout")
+    st = lib().ra_selftest_bulk_timeout(ptr_array([t.data_ptr() for t in sendbufs]),
+                                        ptr_array([t.data_ptr() for t in recvbufs]), count, dtype_code(sendbufs[0]),
+                                        OP_CODES[op], len(sendbufs), ctypes.c_void_p(status.data_ptr()),
+                                        ctypes.c_void_p(_stream_ptr(stream) or None))
+    if st:
+        raise RaError(st, "ra_selftest_bulk_timeout")
 
 
 def ra_vector_bytes() -> int:

@@ -43,28 +43,30 @@ def test_chunk_range_is_floor_definition(ra):
 
 
 @pytest.mark.parametrize("es", [2, 4])
-def test_plan_splits_each_chunk_exactly_once(ra, es):
+@pytest.mark.parametrize("align", [16, 32, 128, 512])
+def test_plan_splits_each_chunk_exactly_once(ra, es, align):
     vb_bytes = ra.ra_vector_bytes()
     assert vb_bytes in (16, 32)
-    v = vb_bytes // es
+    if align < vb_bytes:
+        return
+    v, a = vb_bytes // es, align // es
     for n in (1, 2, 3, 5, 7, 8, 16, 64):
-        for count in list(range(0, 70)) + [1003, 4096, 1_000_003]:
-            for phase in range(0, vb_bytes, es):
+        for count in list(range(0, 70, 3)) + [1003, 4096, 1_000_003]:
+            for phase in range(0, align, max(es, align // 8)):
                 covered = 0
-                head = ((vb_bytes - phase) % vb_bytes) // es
+                head = ((align - phase) % align) // es
                 for c in range(n):
-                    b, e, vb, ve = ra.ra_plan_chunk(count, n, c, es, phase)
+                    b, e, vb, ve = ra.ra_plan_chunk(count, n, c, es, phase, align)
                     assert (b, e) == (c * count // n, (c + 1) * count // n)
                     assert b <= vb <= ve <= e
+                    # the first aligned grid point at or after b
+                    first = head if b <= head else head + -(-(b - head) // a) * a
                     if ve > vb:
-                        assert (vb - head) % v == 0 and (ve - vb) % v == 0 and vb >= head
-                        # maximal: fewer than V elements at either end of the chunk
-                        assert vb - b < v and e - ve < v
+                        assert vb == first and (ve - vb) % v == 0
+                        assert e - ve < v  # runs to the last whole vector
                     else:
                         assert vb == ve == b
-                        # no whole vector fits on the grid inside the chunk
-                        first = head if b <= head else head + -(-(b - head) // v) * v
-                        assert first + v > e
+                        assert first + v > e  # no whole vector fits after the aligned start
                     covered += e - b
                 assert covered == count
 
@@ -74,6 +76,10 @@ def test_plan_rejects_bad_phase(ra):
         ra.ra_plan_chunk(100, 4, 0, 4, 2)  # phase not a multiple of the element size
     with pytest.raises(ra.RaError):
         ra.ra_plan_chunk(100, 4, 0, 3, 0)
+    with pytest.raises(ra.RaError):
+        ra.ra_plan_chunk(100, 4, 0, 4, 0, 48)  # alignment not a power of two
+    with pytest.raises(ra.RaError):
+        ra.ra_plan_chunk(100, 4, 0, 4, 16, 16)  # phase beyond the alignment
 
 
 # Fake, never-dereferenced device addresses: every case below is rejected on the
@@ -112,6 +118,17 @@ def test_ex_options(ra):
         assert ra.call_ex(name, s[:3], d[:3], 1000, 0, 0, 3, 2, 0, 0) == ra.RA_ERR_UNSUPPORTED  # halving, N=3
         assert ra.call_ex(name, s, d, 1000, 2, 0, 4, 1, 1, 0) == ra.RA_ERR_UNSUPPORTED  # fp32 accum + tree
         assert ra.call_ex(name, s, d, 0, 0, 0, 4, 0, 1, 0) == ra.RA_SUCCESS
+    # the bulk engine: needs a status word, covers the ring all-reduce with dtype accumulation up to 16 ranks
+    status = BASE + 512 * MB
+    assert ra.call_ex("ra_allreduce_ex", s, d, 1000, 0, 0, 4, 0, 0, 0, engine=1) == ra.RA_ERR_INVALID_ARG
+    assert ra.call_ex("ra_allreduce_ex", s, d, 1000, 0, 0, 4, 0, 0, 0, engine=5, status=status) == ra.RA_ERR_INVALID_ARG
+    assert ra.call_ex("ra_reduce_scatter_ex", s, d, 1000, 0, 0, 4, 0, 0, 0, engine=1, status=status) == \
+        ra.RA_ERR_UNSUPPORTED
+    assert ra.call_ex("ra_allreduce_ex", s, d, 1000, 2, 0, 4, 1, 0, 0, engine=1, status=status) == ra.RA_ERR_UNSUPPORTED
+    assert ra.call_ex("ra_allreduce_ex", s, d, 1000, 2, 0, 4, 0, 1, 0, engine=1, status=status) == ra.RA_ERR_UNSUPPORTED
+    s20, d20 = bufs(20), bufs(20, base=BASE + 128 * MB)
+    assert ra.call_ex("ra_allreduce_ex", s20, d20, 1000, 0, 0, 20, 0, 0, 0, engine=1, status=status) == \
+        ra.RA_ERR_UNSUPPORTED
     # NULL options = defaults
     f = ra.lib().ra_allreduce_ex
     assert f(ra.ptr_array(s), ra.ptr_array(d), 0, 0, 0, 4, None, None) == ra.RA_SUCCESS

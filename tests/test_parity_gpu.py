@@ -578,3 +578,60 @@ def test_sm_budget_changes_nothing_but_speed(ra):
         ra.ra_allreduce_ex(sends, recvs, "avg", max_sms=max_sms)
         torch.cuda.synchronize()
         assert all(to_host(r, "bf16").tobytes() == b.tobytes() for r, b in zip(recvs, base))
+
+
+# ---------------------------------------------------------------------------
+# the bulk engine (TMA-staged loads): same bits as the register engine, bounded waits
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("f32", "avg"), ("bf16", "avg"), ("f16", "prod"),
+                                      ("i32", "max"), ("bf16", "min")])
+def test_bulk_engine(ra, dtype, op):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for n, length in ((1, 100), (2, 1 << 16), (3, 3 * 4096 * 7 + 11), (5, 1003), (8, (1 << 20) + 13),
+                      (16, 16 * 2048 * 5 + 3)):
+        xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=n + 90)
+        want, _, _ = oracle.allreduce(xs, op, dtype)
+        for max_sms, inplace in ((0, False), (16, False), (0, True)):
+            sends = [to_device(x, dtype) for x in xs]
+            recvs = sends if inplace else [torch.empty_like(s) for s in sends]
+            ra.ra_allreduce_ex(sends, recvs, op, engine="bulk", status=status, max_sms=max_sms)
+            torch.cuda.synchronize()
+            for r in range(n):
+                assert_same_bits(to_host(recvs[r], dtype), want[r], dtype,
+                                 f"bulk n={n} L={length} sms={max_sms} inplace={inplace} rank {r}")
+    assert status.item() == 0
+
+
+def test_bulk_engine_full_size(ra):
+    n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_f32_avg_64m"]
+    xs = inputs.rank_buffers(n, length, dtype, dist)
+    sends = [to_device(x, dtype) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ra.ra_allreduce_ex(sends, recvs, op, engine="bulk", status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for r in range(1, n):
+        assert torch.equal(recvs[r], recvs[0])
+    idx = sample_indices(length, n)
+    got = to_host(recvs[0][torch.from_numpy(idx).cuda()], dtype)
+    assert_same_bits(got, oracle.fold_at(xs, op, dtype, idx), dtype, "bulk full size sampled")
+
+
+def test_bulk_wait_runs_out_and_reports(ra):
+    # one tile's bulk copies are withheld: the consumers' bounded wait gives up after 1 s, the kernel
+    # records the code in the status word and finishes; the context stays usable
+    n, length = 4, 4 * 1024 * 8
+    xs = inputs.rank_buffers(n, length, "f32", ("normal", 1.0), seed_base=3)
+    sends = [to_device(x, "f32") for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ra.ra_selftest_bulk_timeout(sends, recvs, status)
+    torch.cuda.synchronize()
+    assert status.item() in (1, 2)
+    want, _, _ = oracle.allreduce(xs, "sum", "f32")
+    status.zero_()
+    ra.ra_allreduce_ex(sends, recvs, "sum", engine="bulk", status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert_same_bits(to_host(recvs[1], "f32"), want[1], "f32", "after the self-test")
