@@ -70,7 +70,8 @@ typedef enum {
   RA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, nranks outside [1, 64], bad enum, count too big */
   RA_ERR_UNSUPPORTED = 2, /* a dtype/op pair this build does not provide */
   RA_ERR_ALIAS = 3,       /* buffers overlap other than in the allowed in-place layout */
-  RA_ERR_CUDA = 4         /* the CUDA launch failed; see ra_last_cuda_error() */
+  RA_ERR_CUDA = 4,        /* the CUDA launch failed; see ra_last_cuda_error() */
+  RA_ERR_SCRATCH_LIMIT = 5 /* ra_allreduce_bulk_noalloc: nranks above RA_NOALLOC_STATUS_WORDS */
 } ra_status_t;
 
 typedef enum { RA_FLOAT32 = 0, RA_FLOAT16 = 1, RA_BFLOAT16 = 2, RA_INT32 = 3 } ra_dtype_t;
@@ -256,6 +257,57 @@ ra_status_t ra_selftest_bulk_timeout(const void* const* sendbufs, void* const* r
 /* Bytes per vector access of this build's kernels (16 or 32): the address
  * phase (address mod this) the buffers must share for the vector path. */
 int ra_vector_bytes(void);
+
+/* Status words held by the library for ra_allreduce_bulk_noalloc: one per chunk. */
+#define RA_NOALLOC_STATUS_WORDS 16
+
+/*
+ * The RA_ENGINE_BULK all-reduce for a caller that cannot allocate device
+ * memory. The web pages have no counterpart: this is an interface of this
+ * library only. Result bits, buffers, in-place rules and other errors are
+ * those of ra_allreduce_ex with RA_ENGINE_BULK; the difference is where the
+ * status words live. ra_allreduce_ex wants a device int from the caller;
+ * here the library keeps RA_NOALLOC_STATUS_WORDS ints of its own, a fixed
+ * array inside libra.so's device image, and the call allocates nothing.
+ *
+ * Who needs this: a caller whose device memory is all held by another
+ * allocator (a framework's caching pool), which has no device allocation
+ * call of its own to use and would only fragment that pool with a stray
+ * cudaMalloc; a caller between the kernels of a training step, where
+ * cudaFree would make the host wait for the whole device, including the
+ * compute that the bulk engine is meant to run beside; and a host program
+ * that all-reduces pinned host buffers and owns no device memory at all.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * device address of the array (cudaGetSymbolAddress) and keeps it for later
+ * calls on that device; a failed lookup returns RA_ERR_CUDA. The lookup can
+ * load the library's kernels onto the device, so make the first call before
+ * any stream capture begins.
+ *
+ * Each call enqueues on `stream`: a clear of words [0, nranks) of the array;
+ * the kernel, whose CTAs for chunk c record in word c the code of a bounded
+ * wait that gave up (1: a bulk copy did not land within 1 s; 2: a stage was
+ * not released within 1 s); and, if chunk_status is not NULL, a copy of
+ * those nranks words to chunk_status (device memory or host memory, nranks
+ * ints, caller-owned; pageable host memory makes the call wait until the
+ * kernel has finished). Read chunk_status once the stream has passed the
+ * call: 0 everywhere means every chunk finished. max_sms as in ra_options_t.
+ * count == 0 enqueues nothing and leaves chunk_status untouched.
+ *
+ * Limit: nranks must be at most RA_NOALLOC_STATUS_WORDS (16, the bulk
+ * engine's own limit); a larger nranks (up to RA_MAX_RANKS) returns
+ * RA_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *
+ * Concurrency: each device has one copy of the array, shared by all calls on
+ * that device. Two calls in flight at once there (on different streams, or
+ * from different threads) race on it: one call's clear can erase the
+ * other's codes, and a copy can return the other's codes. The reduced
+ * buffers are not affected. Calls on one stream run one after the other and
+ * do not race.
+ */
+ra_status_t ra_allreduce_bulk_noalloc(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                      ra_dtype_t dtype, ra_op_t op, int nranks, int max_sms, int* chunk_status,
+                                      void* stream);
 
 #ifdef __cplusplus
 }

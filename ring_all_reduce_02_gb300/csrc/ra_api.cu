@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/ra.h"
 #include "ra_ag_shape.h"
 #include "ra_bulk.cuh"
@@ -183,10 +185,11 @@ const ra_options_t kDefaultOptions = {RA_ORDER_RING, RA_ACCUM_DTYPE, 0, RA_ENGIN
 constexpr size_t kBulkSmemBudget = 200 * 1024;
 
 ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* status, void* stream,
-                     int withhold_first = 0) {
+                     int withhold_first = 0, uint32_t status_stride = 0) {
   ra::BulkArgs b;
   b.base = a;
   b.status = status;
+  b.status_stride = status_stride;
   b.withhold_first = withhold_first;
   const int n = a.nranks;
   b.tile_vecs = n <= 8 ? 256 : 128;  // 4 KB or 2 KB per rank per stage (16-byte vectors)
@@ -510,6 +513,7 @@ const char* ra_status_string(ra_status_t status) {
     case RA_ERR_UNSUPPORTED: return "unsupported dtype/op/order";
     case RA_ERR_ALIAS: return "buffers overlap outside the in-place layout";
     case RA_ERR_CUDA: return "CUDA launch failed";
+    case RA_ERR_SCRATCH_LIMIT: return "nranks exceeds the library's status words (RA_NOALLOC_STATUS_WORDS)";
   }
   return "unknown status";
 }
@@ -529,3 +533,61 @@ ra_status_t ra_selftest_bulk_timeout(const void* const* sendbufs, void* const* r
 }
 
 }  // extern "C"
+
+// ---- the bulk all-reduce without caller scratch ------------------------------
+// The status words of ra_allreduce_bulk_noalloc: one per chunk, part of the
+// module's device image, so no call allocates them. One copy per device; calls
+// in flight at once on one device share it (see the declaration in ra.h).
+namespace {
+
+static __device__ __align__(256) int g_noalloc_status[RA_NOALLOC_STATUS_WORDS];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int* g_noalloc_ptr[kMaxDevices] = {};
+
+// The array's device address on the current device, looked up on the first
+// call there and kept.
+ra_status_t noalloc_status_words(int** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_failed(err);
+  if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_noalloc_status);
+    if (err != cudaSuccess) return cuda_failed(err);
+    g_noalloc_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return RA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" ra_status_t ra_allreduce_bulk_noalloc(const void* const* sendbufs, void* const* recvbufs,
+                                                 size_t count, ra_dtype_t dtype, ra_op_t op, int nranks,
+                                                 int max_sms, int* chunk_status, void* stream) {
+  if (nranks < 1 || nranks > RA_MAX_RANKS || max_sms < 0) return RA_ERR_INVALID_ARG;
+  if (nranks > RA_NOALLOC_STATUS_WORDS) return RA_ERR_SCRATCH_LIMIT;
+  ra::Args a;
+  ra_status_t st = prepare(ra::KIND_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, nranks, &a);
+  if (st != RA_SUCCESS) return st;
+  if (count == 0) return RA_SUCCESS;
+  if (!a.vec_ok) return RA_ERR_UNSUPPORTED;
+  int* words = nullptr;
+  st = noalloc_status_words(&words);
+  if (st != RA_SUCCESS) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)nranks * sizeof(int);
+  cudaError_t err = cudaMemsetAsync(words, 0, bytes, s);
+  if (err != cudaSuccess) return cuda_failed(err);
+  st = run_bulk(a, dtype, op, max_sms, words, stream, /*withhold_first=*/0, /*status_stride=*/1);
+  if (st != RA_SUCCESS) return st;
+  if (chunk_status != nullptr) {
+    err = cudaMemcpyAsync(chunk_status, words, bytes, cudaMemcpyDefault, s);
+    if (err != cudaSuccess) return cuda_failed(err);
+  }
+  return RA_SUCCESS;
+}

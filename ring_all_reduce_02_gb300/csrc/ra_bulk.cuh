@@ -30,7 +30,8 @@ constexpr int kBulkErrEmpty = 2;                   // the consumers did not rele
 
 struct BulkArgs {
   Args base;
-  int* status;        // device word; 0 = fine, else the first error code seen
+  int* status;        // device words; 0 = fine, else the first error code seen
+  uint32_t status_stride;  // 0: every chunk reports into status[0]; 1: chunk c into status[c]
   uint32_t tile_vecs;  // vectors per rank per stage (a multiple of kBulkConsumers)
   uint32_t stages;     // stages in the shared-memory ring
   int withhold_first;  // self-test of the bounded waits: CTA (0, 0) never issues its first tile's copies
@@ -90,6 +91,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
   uint64_t* empty = full + S;                          // [S]: consumers done with a stage
   uint8_t* data = smem + 128 * ((2 * S * 8 + 127) / 128);  // [S][n][tile_bytes]
 
+  int* const status = ba.status + (size_t)c * ba.status_stride;
+
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
       for (uint64_t t = first; t < ntiles; t += step, ++issued) {
         const uint32_t s = issued % S;
         if (issued >= S && !mbar_wait(&empty[s], ((issued / S) - 1) & 1)) {
-          record_error(ba.status, kBulkErrEmpty);
+          record_error(status, kBulkErrEmpty);
           ok = false;
           break;
         }
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
       const uint32_t lo = issued > S ? issued - S : 0;
       for (uint32_t i = lo; i < issued; ++i) {
         if (!mbar_wait(&full[i % S], (i / S) & 1)) {
-          record_error(ba.status, kBulkErrFull);
+          record_error(status, kBulkErrFull);
           break;
         }
       }
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
     for (uint64_t t = first; t < ntiles; t += step, ++used) {
       const uint32_t s = used % S;
       if (!mbar_wait(&full[s], (used / S) & 1)) {
-        record_error(ba.status, kBulkErrFull);
+        record_error(status, kBulkErrFull);
         break;
       }
       const uint8_t* tile = data + (size_t)s * n * tile_bytes;

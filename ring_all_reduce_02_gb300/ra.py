@@ -16,7 +16,8 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libra.so")
 
-RA_SUCCESS, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_ALIAS, RA_ERR_CUDA = range(5)
+RA_SUCCESS, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_ALIAS, RA_ERR_CUDA, RA_ERR_SCRATCH_LIMIT = range(6)
+RA_NOALLOC_STATUS_WORDS = 16
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
 OP_CODES = {"sum": 0, "avg": 1, "min": 2, "max": 3, "prod": 4}
 ORDER_CODES = {"ring": 0, "tree": 1, "rabenseifner": 2}
@@ -26,7 +27,8 @@ RA_MAX_RANKS = 64
 # every symbol include/ra.h declares
 EXPORTS = ("ra_allreduce", "ra_reduce_scatter", "ra_allgather", "ra_allreduce_ex", "ra_reduce_scatter_ex",
            "ra_bucket_plan", "ra_allreduce_buckets", "ra_allreduce_ringsteps", "ra_chunk_range", "ra_plan_chunk",
-           "ra_status_string", "ra_last_cuda_error", "ra_vector_bytes", "ra_selftest_bulk_timeout")
+           "ra_status_string", "ra_last_cuda_error", "ra_vector_bytes", "ra_selftest_bulk_timeout",
+           "ra_allreduce_bulk_noalloc")
 ENGINE_CODES = {"registers": 0, "bulk": 1}
 
 
@@ -95,6 +97,8 @@ def lib() -> ctypes.CDLL:
             L.ra_vector_bytes.restype = I
             L.ra_selftest_bulk_timeout.argtypes = [PP, PP, SZ, I, I, I, VP, VP]
             L.ra_selftest_bulk_timeout.restype = I
+            L.ra_allreduce_bulk_noalloc.argtypes = [PP, PP, SZ, I, I, I, I, VP, VP]
+            L.ra_allreduce_bulk_noalloc.restype = I
             _lib = L
     return _lib
 
@@ -303,3 +307,23 @@ def ra_selftest_bulk_timeout(sendbufs, recvbufs, status, op: str = "sum", stream
 
 def ra_vector_bytes() -> int:
     return lib().ra_vector_bytes()
+
+
+def ra_allreduce_bulk_noalloc(sendbufs, recvbufs, op: str = "sum", max_sms: int = 0, chunk_status=None,
+                              stream=None) -> None:
+    """The bulk-engine all-reduce with the status words kept by the library, so no device memory
+    beyond the buffers is needed. ``chunk_status``: optional int32 tensor of nranks words (device or
+    host) that receives each chunk's wait code (0 = finished) once the stream has passed the call."""
+    import torch
+
+    count = _check_full(sendbufs, recvbufs, "ra_allreduce_bulk_noalloc")
+    if chunk_status is not None and (chunk_status.dtype != torch.int32 or not chunk_status.is_contiguous()
+                                     or chunk_status.numel() < len(sendbufs)):
+        raise ValueError("ra_allreduce_bulk_noalloc: chunk_status must be a contiguous int32 tensor of nranks words")
+    cs = chunk_status.data_ptr() if chunk_status is not None else None
+    st = lib().ra_allreduce_bulk_noalloc(ptr_array([t.data_ptr() for t in sendbufs]),
+                                         ptr_array([t.data_ptr() for t in recvbufs]), count,
+                                         dtype_code(sendbufs[0]), OP_CODES[op], len(sendbufs), max_sms,
+                                         ctypes.c_void_p(cs), ctypes.c_void_p(_stream_ptr(stream) or None))
+    if st:
+        raise RaError(st, "ra_allreduce_bulk_noalloc")
