@@ -455,6 +455,87 @@ def run_sweep(args):
 
 
 # ---------------------------------------------------------------------------
+# one call of the library timed alone on a workload's buffers (not the headline):
+# per-kernel rooflines and the command that ncu captures of each kernel run
+# ---------------------------------------------------------------------------
+CALLS = {  # name: (kernel, algorithmic bytes per launch as a multiple of S, the bytes per rank)
+    "allreduce": ("ar_fused_kernel", lambda n: 2 * n),
+    "reduce_scatter": ("rs_fused_kernel", lambda n: n + 1),
+    "allgather": ("ag_tma_store_kernel", lambda n: n + 1),
+    "allreduce_bulk": ("ar_bulk_kernel", lambda n: 2 * n),
+    "allreduce_fp32acc": ("ar_fused_kernel (fp32 partials)", lambda n: 2 * n),
+    "allreduce_tree": ("ordered_kernel", lambda n: 2 * n),
+    "allreduce_rabenseifner": ("ordered_kernel", lambda n: 2 * n),
+}
+
+
+def run_call(args):
+    import torch
+
+    from ring_all_reduce_02_gb300 import build, ra
+
+    build.build()
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    n, length, dtype, op, _ = inputs.WORKLOADS[args.workload]
+    es = inputs.ELEM_SIZE[dtype]
+    s_bytes = length * es
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "i32": torch.int32}[dtype]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    sends = [torch.empty(length, dtype=torch.float32, device="cuda").normal_(generator=g).to(tdt) for _ in range(n)]
+    recvs = [torch.empty_like(x) for x in sends]
+    bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+    shards = [x[b:e].clone() for x, (b, e) in zip(sends, bounds)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    name = args.call
+    fn = {
+        "allreduce": lambda: ra.ra_allreduce(sends, recvs, op, stream=stream),
+        "reduce_scatter": lambda: ra.ra_reduce_scatter(sends, shards, op, stream=stream),
+        "allgather": lambda: ra.ra_allgather(shards, recvs, stream=stream),
+        "allreduce_bulk": lambda: ra.ra_allreduce_ex(sends, recvs, op, engine="bulk", status=status, stream=stream),
+        "allreduce_fp32acc": lambda: ra.ra_allreduce_ex(sends, recvs, op, accum="fp32", stream=stream),
+        "allreduce_tree": lambda: ra.ra_allreduce_ex(sends, recvs, op, order="tree", stream=stream),
+        "allreduce_rabenseifner": lambda: ra.ra_allreduce_ex(sends, recvs, op, order="rabenseifner", stream=stream),
+    }[name]
+    kernel, mult = CALLS[name]
+    hbm_bytes = mult(n) * s_bytes
+    for _ in range(args.warmup):
+        fn()
+    sampler = ClockSampler(dev).start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for k in range(args.steps):
+        starts[k].record(stream)
+        fn()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    per = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    mean_ms = sum(per) / len(per)
+    peak, peak_kind = measured_peaks()
+    achieved = hbm_bytes / (mean_ms * 1e-3) / GB
+    print(json.dumps({
+        "mode": "call", "call": name, "kernel": kernel, "workload": args.workload, "nranks": n, "count": length,
+        "dtype": dtype, "op": op, "steps": args.steps, "warmup": args.warmup,
+        "inputs": "seeded normal(0, 1) drawn on the device",
+        "l2": f"{hbm_bytes / GB:.2f} GB moved per launch vs ~0.13 GB L2",
+        "algorithmic_bytes_per_launch": hbm_bytes,
+        "launch_ms": {"mean": round(mean_ms, 5), "min": round(min(per), 5), "median": round(statistics.median(per), 5)},
+        "achieved_GBps": round(achieved, 1), "peak": peak, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+        "frac": round(achieved / peak, 4), "status": int(status.item()),
+        "algbw_GBps": round(s_bytes / (mean_ms * 1e-3) / GB, 3),
+        "clocks": sampler.summary(t_wall0, t_wall1)}), flush=True)
+    return 0 if status.item() == 0 else 1
+
+
+# ---------------------------------------------------------------------------
 # bucketed all-reduce overlapped with a synthetic backward pass (not the headline)
 # ---------------------------------------------------------------------------
 def run_overlap(args):
@@ -553,6 +634,8 @@ def main():
     ap.add_argument("--sweep-max", type=int, default=0, help="largest count in the sweep (0 = all)")
     ap.add_argument("--overlap", action="store_true", help="bucketed all-reduce beside a synthetic backward")
     ap.add_argument("--overlap-tokens", type=int, default=2048)
+    ap.add_argument("--call", default=None, choices=sorted(CALLS),
+                    help="time one call alone on the workload (per-kernel roofline; not the headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -562,6 +645,8 @@ def main():
         return run_sweep(args)
     if args.overlap:
         return run_overlap(args)
+    if args.call:
+        return run_call(args)
     return run_ours(args)
 
 

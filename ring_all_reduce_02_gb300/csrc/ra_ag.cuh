@@ -1,0 +1,143 @@
+// The all-gather kernels and their plan: compact chunk c (src[c]) goes to
+// every destination at [b0, b1) — one read and N writes per element
+// (infra-guide "All-Gather"; tirogla "How it works", the all-gather phase).
+//
+// HBM writes bound this kernel. On GB300 a pure stream of stores from the SMs
+// peaks near 6.4 TB/s (94% of the copy bandwidth) whatever the store width or
+// cache hint, against about 7.2 TB/s for reads. Two kernels:
+//  - ag_copy_kernel (ra_kernels.cuh): every thread loads vectors into
+//    registers and stores each to the N destinations;
+//  - ag_tma_store_kernel (below): the threads load a tile into shared memory
+//    and one thread hands it to the Tensor Memory Accelerator as N bulk
+//    stores (cp.async.bulk shared -> global, 8 KB contiguous per destination),
+//    double-buffered so the next tile loads while the last one is written.
+// The planner picks the kernel and the CTAs per SM from N.
+#pragma once
+
+#include "ra_bulk.cuh"
+#include "ra_kernels.cuh"
+
+namespace ra {
+
+constexpr int kAgThreads = 256;
+using AgShape = Shape<kAgThreads, 2, 1, 1>;  // the register kernel
+
+constexpr uint32_t kAgStages = 2;
+
+enum AgKernel { AG_REGISTERS = 0, AG_TMA_STORE = 1 };
+constexpr int kShapeAgBase = 100;  // Args::shape of an all-gather launch: kShapeAgBase + AgKernel
+
+struct AgPlan {
+  int kernel;         // AgKernel
+  int unroll;         // AG_TMA_STORE: vectors per thread per tile (1 or 2: 8 or 16 KB tiles at 32-byte vectors)
+  int blocks_per_sm;  // resident CTAs per SM the grid is sized for
+};
+
+// Chosen from a sweep on GB300 (fp32, 1 GiB over all ranks, fraction of the
+// copy bandwidth): the tiles in flight per SM that keep HBM busiest shrink as
+// N grows, because the reads are 1/(N+1) of the traffic. 32 KB per SM at
+// N <= 3 (97% at N = 2, 93% at N = 3), 16 KB at N = 4..7 (88-94%), 8 KB from
+// N = 8 (92% at N = 8, 90% at N = 12, 87% at N = 16). The register kernel
+// measured 84-91% at its best shape.
+inline AgPlan ag_plan_for(int nranks) {
+#ifdef RA_AG_TUNE_KERNEL  // tuning sweeps: one plan for every rank count
+  (void)nranks;
+  return {RA_AG_TUNE_KERNEL, RA_AG_TUNE_UNROLL, RA_AG_TUNE_BPS};
+#else
+  if (nranks <= 2) return {AG_TMA_STORE, 1, 4};
+  if (nranks == 3) return {AG_TMA_STORE, 2, 2};
+  if (nranks <= 5) return {AG_TMA_STORE, 1, 2};
+  if (nranks <= 7) return {AG_TMA_STORE, 2, 1};
+  return {AG_TMA_STORE, 1, 1};
+#endif
+}
+
+template <int kUnroll>
+__host__ __device__ constexpr uint32_t ag_tile_bytes() {
+  return (uint32_t)kAgThreads * kUnroll * kVecBytes;  // per destination
+}
+
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Vector at byte offset off (of the destination layout) from the compact
+// chunk that starts at element b0: one vector load when the chunk shares the
+// destinations' phase, element loads otherwise.
+template <int DT>
+__device__ __forceinline__ Vec ag_load(const void* in, bool in_vec, uint64_t off, uint64_t b0) {
+  constexpr int ES = Elem<DT>::kSize;
+  if (in_vec) return ld_vec(static_cast<const char*>(in) + off - b0 * ES);
+  Vec v;
+  const uint64_t i = off / ES - b0;
+#pragma unroll
+  for (int k = 0; k < kVecWords; ++k) {
+    if constexpr (ES == 4) {
+      v.w[k] = ld_elem<DT>(in, i + k);
+    } else {
+      v.w[k] = ld_elem<DT>(in, i + 2 * k) | (ld_elem<DT>(in, i + 2 * k + 1) << 16);
+    }
+  }
+  return v;
+}
+
+// grid (CTAs per chunk, N), kAgThreads threads, kAgStages * ag_tile_bytes<kUnroll>()
+// of dynamic shared memory. The chunk's whole tiles go through shared memory and
+// bulk stores; the leftover vectors and the edge elements take plain stores.
+template <int DT, int kUnroll>
+__global__ void __launch_bounds__(kAgThreads) ag_tma_store_kernel(const __grid_constant__ Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int V = Elem<DT>::kPerVec;
+  constexpr int ES = Elem<DT>::kSize;
+  constexpr uint32_t TV = (uint32_t)kAgThreads * kUnroll;  // vectors per tile
+  constexpr uint32_t TB = ag_tile_bytes<kUnroll>();
+  const int n = a.nranks, c = blockIdx.y;
+  const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
+  uint64_t vb = b0, ve = b0;
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
+  const uint64_t nv = (ve - vb) / V;
+  const uint64_t ntiles = nv / TV;
+  const void* in = a.src[c];
+  const bool in_vec = (a.compact_aligned >> c) & 1u;
+
+  uint32_t it = 0;
+  for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    Vec v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      v[u] = ag_load<DT>(in, in_vec, (vb + (t * TV + (uint64_t)u * kAgThreads + threadIdx.x) * V) * ES, b0);
+    uint8_t* stage = smem + (it % kAgStages) * TB;
+    // the stage was last handed to bulk stores kAgStages tiles ago: wait until they have read it
+    if (it >= kAgStages && threadIdx.x == 0)
+      asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kAgStages - 1) : "memory");
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      *reinterpret_cast<Vec*>(stage + ((uint32_t)u * kAgThreads + threadIdx.x) * kVecBytes) = v[u];
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic-proxy writes -> bulk copies
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint64_t off = (vb + t * TV * V) * ES;
+      for (int r = 0; r < n; ++r) bulk_store(static_cast<char*>(a.dst[r]) + off, stage, TB);
+      bulk_commit();
+    }
+  }
+
+  for (uint64_t j = ntiles * TV + (uint64_t)blockIdx.x * kAgThreads + threadIdx.x; j < nv;
+       j += (uint64_t)gridDim.x * kAgThreads) {
+    const uint64_t off = (vb + j * V) * ES;
+    const Vec x = ag_load<DT>(in, in_vec, off, b0);
+    for (int r = 0; r < n; ++r) st_vec(static_cast<char*>(a.dst[r]) + off, x);
+  }
+  for_each_edge_elem<kAgThreads>(b0, vb, ve, b1, [&](uint64_t i) {
+    const uint32_t x = ld_elem<DT>(in, i - b0);
+    for (int r = 0; r < n; ++r) st_elem<DT>(a.dst[r], i, x);
+  });
+  // shared memory must outlive the bulk stores that read it
+  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+}  // namespace ra

@@ -9,7 +9,7 @@
 #include <mutex>
 
 #include "../../include/ra.h"
-#include "ra_ag_shape.h"
+#include "ra_ag.cuh"
 #include "ra_bulk.cuh"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
@@ -134,9 +134,6 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
   return RA_SUCCESS;
 }
 
-// Launch-shape id of the all-gather kernel (its shape lives in ra_ag_shape.h).
-constexpr int kShapeAllGather = 100;
-
 // SMs the launch may fill: all of them, or the caller's budget (max_sms > 0)
 // when other work runs beside the collective.
 ra_status_t sm_budget(int max_sms, int* sms) {
@@ -153,8 +150,10 @@ ra_status_t sm_budget(int max_sms, int* sms) {
 // of the launch shape on the SM budget.
 ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3* grid) {
   int threads, per_thread, min_blocks, sms = 0;
-  if (shape == kShapeAllGather) {
-    threads = ra::AgShape::kThreads, per_thread = ra::AgShape::kUnroll, min_blocks = ra::AgShape::kMinBlocks;
+  if (shape >= ra::kShapeAgBase) {
+    const ra::AgPlan p = ra::ag_plan_for(a.nranks);
+    threads = ra::kAgThreads, min_blocks = p.blocks_per_sm;
+    per_thread = p.kernel == ra::AG_TMA_STORE ? p.unroll : ra::AgShape::kUnroll;
   } else {
     ra::shape_params(shape, &threads, &per_thread, &min_blocks);
   }
@@ -192,7 +191,10 @@ ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* sta
   b.status_stride = status_stride;
   b.withhold_first = withhold_first;
   const int n = a.nranks;
-  b.tile_vecs = n <= 8 ? 256 : 128;  // 4 KB or 2 KB per rank per stage (16-byte vectors)
+  // 4 KB per rank per stage (2 KB above 8 ranks), and at least one vector per consumer thread
+  uint32_t tv = (n <= 8 ? 4096u : 2048u) / (uint32_t)ra::kVecBytes;
+  if (tv < (uint32_t)ra::kBulkConsumers) tv = ra::kBulkConsumers;
+  b.tile_vecs = tv;
   const size_t stage_bytes = (size_t)n * b.tile_vecs * ra::kVecBytes;
   size_t stages = kBulkSmemBudget / stage_bytes;
   if (stages > 8) stages = 8;
@@ -313,7 +315,7 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   }
   if (order != RA_ORDER_RING) return run_ordered(kind, a, dtype, op, order, max_sms, stream);
   a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
-  a.shape = kind == ra::KIND_ALLGATHER ? kShapeAllGather
+  a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ra::ag_plan_for(nranks).kernel
                                        : ra::shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0);
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);

@@ -35,12 +35,13 @@ namespace ra {
 // Launch shapes of the fused AR/RS kernels. How many bytes a thread keeps in
 // flight is N loads x kUnroll vectors, so the rank count decides how many
 // threads per SM and vectors per thread keep HBM busiest; the host planner
-// picks the shape from N. Measured on GB300 (fraction of the copy bandwidth,
-// fp32 all-reduce of 0.5-2 GiB per rank): N = 2: 98% with 128 threads x 2
-// vectors at 8 CTAs/SM (88% with the N = 4 shape); N = 3 and 4: 90% and 97%
-// with 256 x 8 at 1 CTA/SM; N = 5: 87% with 256 x 2 at 2 CTAs/SM; N = 6..11:
-// 256 x 4 at 1 CTA/SM with loads of 8 ranks in flight (98% at N = 8); N >= 12:
-// the same with batches of 4 ranks (97% at N = 16 against 95%).
+// picks the shape from N. Measured on GB300 with 32-byte vectors (fraction of
+// the copy bandwidth, fp32, 1 GiB over all ranks): all-reduce N <= 2: 96% with
+// 128 threads x 1 vector at 8 CTAs/SM; N = 3: 98% with 256 x 4 at 1 CTA/SM;
+// N = 4..7: 95-99% with 256 x 1 at 2 CTAs/SM (the wide shape: 90-92% at
+// N = 6, 7); N >= 8: 256 x 2 at 1 CTA/SM (99.5% at N = 8, 97% at N = 12 and
+// 16). Reduce-scatter reads N values per element and writes one, and runs at
+// 98-102% with the small shape at every N.
 // 0: the CTAs of a chunk interleave (grid-stride); 1: each CTA streams one
 // contiguous slab of the chunk.
 #ifndef RA_SCHEDULE
@@ -55,33 +56,27 @@ struct Shape {
   static constexpr int kBatch = BATCH;           // ranks whose loads are in flight together
 };
 #ifndef RA_TUNE_SHAPE
-using ShapeN2 = Shape<128, 8, 2, 4>;    // nranks 1..2
-using ShapeN4 = Shape<256, 1, 8, 4>;    // nranks 3..4
-using ShapeN5 = Shape<256, 2, 2, 4>;    // nranks 5
-using ShapeW8 = Shape<256, 1, 4, 8>;    // nranks 6..11
-using ShapeW16 = Shape<256, 1, 4, 4>;   // nranks 12..64
+using ShapeS = Shape<128, 8, 1, 4>;   // all-reduce nranks 1..2; every reduce-scatter
+using ShapeN3 = Shape<256, 1, 4, 4>;  // all-reduce nranks 3
+using ShapeM = Shape<256, 2, 1, 4>;   // all-reduce nranks 4..7; fp32 partials where ShapeS would spill
+using ShapeW = Shape<256, 1, 2, 4>;   // all-reduce nranks >= 8
 #else  // tuning sweeps: one shape (RA_TUNE_T, _MB, _U, _B) for every rank count
-using ShapeN2 = Shape<RA_TUNE_T, RA_TUNE_MB, RA_TUNE_U, RA_TUNE_B>;
-using ShapeN4 = ShapeN2;
-using ShapeN5 = ShapeN2;
-using ShapeW8 = ShapeN2;
-using ShapeW16 = ShapeN2;
+using ShapeS = Shape<RA_TUNE_T, RA_TUNE_MB, RA_TUNE_U, RA_TUNE_B>;
+using ShapeN3 = ShapeS;
+using ShapeM = ShapeS;
+using ShapeW = ShapeS;
 #endif
-using StepShape = Shape<256, 2, 1, 1>;  // ring-step and all-gather kernels
-enum ShapeId { SHAPE_N2 = 0, SHAPE_N4 = 1, SHAPE_N5 = 2, SHAPE_W8 = 3, SHAPE_W16 = 4, SHAPE_STEP = 5 };
+using StepShape = Shape<256, 2, 1, 1>;  // ring-step kernels
+enum ShapeId { SHAPE_S = 0, SHAPE_N3 = 1, SHAPE_M = 2, SHAPE_W = 3, SHAPE_STEP = 5 };
 
-// The fused shape for a call. Reduce-scatter writes one compact chunk instead
-// of N copies and does best with the N = 2 shape up to N = 4 (103% of the copy
-// bandwidth at N = 4); fp32 accumulation at N <= 5 uses the N = 5 shape, whose
-// register budget holds the fp32 partials without spilling.
+// The fused shape for a call. fp32 partials (fp16/bf16 with fp32
+// accumulation) need more registers than ShapeS leaves, so those calls take
+// ShapeM where the plain call would take ShapeS.
 inline int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false) {
-  if (reduce_scatter && nranks <= 4) return acc32 ? SHAPE_N5 : SHAPE_N2;
-  if (acc32 && nranks <= 5) return SHAPE_N5;
-  if (nranks <= 2) return SHAPE_N2;
-  if (nranks <= 4) return SHAPE_N4;
-  if (nranks == 5) return SHAPE_N5;
-  if (nranks < 12) return SHAPE_W8;
-  return SHAPE_W16;
+  if (reduce_scatter || nranks <= 2) return acc32 ? SHAPE_M : SHAPE_S;
+  if (nranks == 3) return acc32 ? SHAPE_M : SHAPE_N3;
+  if (nranks <= 7) return SHAPE_M;
+  return SHAPE_W;
 }
 
 enum Kind {
@@ -472,17 +467,18 @@ template <int DT, int OP, bool ACC32>
 cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
   const bool rs = kind == KIND_REDUCE_SCATTER;
   switch (a.shape) {
-    case SHAPE_N2:
-      if constexpr (!ACC32) return launch_fused_shape<DT, OP, false, ShapeN2>(kind, a, grid, s);
+    case SHAPE_S:
+      if constexpr (!ACC32) return launch_fused_shape<DT, OP, false, ShapeS>(kind, a, grid, s);
       break;
-    case SHAPE_N4:
+    case SHAPE_N3:
       if constexpr (!ACC32) {
-        if (!rs) return launch_ar<DT, OP, false, ShapeN4>(a, grid, s);
+        if (!rs) return launch_ar<DT, OP, false, ShapeN3>(a, grid, s);
       }
       break;
-    case SHAPE_N5: return launch_fused_shape<DT, OP, ACC32, ShapeN5>(kind, a, grid, s);
-    case SHAPE_W8: return launch_fused_shape<DT, OP, ACC32, ShapeW8>(kind, a, grid, s);
-    case SHAPE_W16: return launch_fused_shape<DT, OP, ACC32, ShapeW16>(kind, a, grid, s);
+    case SHAPE_M: return launch_fused_shape<DT, OP, ACC32, ShapeM>(kind, a, grid, s);
+    case SHAPE_W:
+      if (!rs) return launch_ar<DT, OP, ACC32, ShapeW>(a, grid, s);
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -504,11 +500,10 @@ inline void shape_params_of(int* threads, int* unroll, int* min_blocks) {
 }
 inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) {
   switch (shape) {
-    case SHAPE_N2: return shape_params_of<ShapeN2>(threads, unroll, min_blocks);
-    case SHAPE_N4: return shape_params_of<ShapeN4>(threads, unroll, min_blocks);
-    case SHAPE_N5: return shape_params_of<ShapeN5>(threads, unroll, min_blocks);
-    case SHAPE_W8: return shape_params_of<ShapeW8>(threads, unroll, min_blocks);
-    case SHAPE_W16: return shape_params_of<ShapeW16>(threads, unroll, min_blocks);
+    case SHAPE_S: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
+    case SHAPE_N3: return shape_params_of<ShapeN3>(threads, unroll, min_blocks);
+    case SHAPE_M: return shape_params_of<ShapeM>(threads, unroll, min_blocks);
+    case SHAPE_W: return shape_params_of<ShapeW>(threads, unroll, min_blocks);
     default: return shape_params_of<StepShape>(threads, unroll, min_blocks);
   }
 }

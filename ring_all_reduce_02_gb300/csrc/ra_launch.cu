@@ -1,6 +1,6 @@
 // Dispatch to the (dtype, op) slices of ra_launch_op.cu, plus the
 // op-independent kernels (all-gather and the ring's all-gather step).
-#include "ra_ag_shape.h"
+#include "ra_ag.cuh"
 #include "ra_bulk.cuh"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
@@ -34,8 +34,15 @@ const BulkSliceFn kBulkSlices[4][5] = {RA_BROW(0), RA_BROW(1), RA_BROW(2), RA_BR
 
 template <int DT>
 cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
-  if (kind == KIND_ALLGATHER) ag_copy_kernel<DT, AgShape><<<grid, AgShape::kThreads, 0, s>>>(a);
-  else ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
+  if (kind == KIND_ALLGATHER && a.shape == kShapeAgBase + AG_TMA_STORE) {
+    if (ag_plan_for(a.nranks).unroll == 2)
+      ag_tma_store_kernel<DT, 2><<<grid, kAgThreads, kAgStages * ag_tile_bytes<2>(), s>>>(a);
+    else
+      ag_tma_store_kernel<DT, 1><<<grid, kAgThreads, kAgStages * ag_tile_bytes<1>(), s>>>(a);
+  } else if (kind == KIND_ALLGATHER)
+    ag_copy_kernel<DT, AgShape><<<grid, AgShape::kThreads, 0, s>>>(a);
+  else
+    ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

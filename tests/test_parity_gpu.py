@@ -277,7 +277,7 @@ def test_offset_views(ra, dtype):
     xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=9)
     want, _, _ = oracle.allreduce(xs, "avg", dtype)
     es = ELEM_SIZE[dtype]
-    per_vec = 16 // es
+    per_vec = ra.ra_vector_bytes() // es
     for offsets in ([1] * 8, [per_vec - 1] * 8, [0, 1, 2, 3, 0, 1, 2, 3], [0] * 4 + [1] * 4):
         got = run_allreduce(ra, xs, "avg", dtype, offsets=offsets)
         for r in range(n):
