@@ -411,6 +411,9 @@ def run_sweep(args):
             for _ in range(reps):
                 if not resident:
                     flush.zero_()
+                # keep the GPU busy until the launch and both events are queued, so that the
+                # interval holds the kernel alone and none of the host's call overhead
+                torch.cuda._sleep(200_000)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 fn()

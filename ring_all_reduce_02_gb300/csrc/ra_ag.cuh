@@ -84,6 +84,56 @@ __device__ __forceinline__ Vec ag_load(const void* in, bool in_vec, uint64_t off
   return v;
 }
 
+// The whole tiles of one chunk. G = 0: the compact chunk is on the
+// destinations' vector grid and a thread loads kUnroll vectors; G = 2..16: it
+// is off the grid and the CTA reads the tile in G-byte units, consecutive
+// threads on consecutive units. Either way the loads are issued before the
+// wait for the stage, and the stage holds the tile in destination order.
+template <int DT, int kUnroll, uint32_t G>
+__device__ __forceinline__ void ag_tiles(const Args& a, uint8_t* smem, const char* in, uint64_t vb, uint64_t b0,
+                                         uint64_t ntiles) {
+  constexpr int V = Elem<DT>::kPerVec;
+  constexpr int ES = Elem<DT>::kSize;
+  constexpr uint32_t TV = (uint32_t)kAgThreads * kUnroll;  // vectors per tile
+  constexpr uint32_t TB = ag_tile_bytes<kUnroll>();
+  using T = typename UnitT<G == 0 ? 16 : G>::T;
+  constexpr uint32_t K = G == 0 ? kUnroll : TB / (G * kAgThreads);  // loads per thread per tile
+  const int n = a.nranks;
+  uint32_t it = 0;
+  for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    const char* src = in + (vb + t * TV * V - b0) * ES;  // the tile in the compact chunk
+    Vec v[G == 0 ? kUnroll : 1];
+    T w[G == 0 ? 1 : K];
+    if constexpr (G == 0) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) v[u] = ld_vec(src + ((uint32_t)u * kAgThreads + threadIdx.x) * kVecBytes);
+    } else {
+#pragma unroll
+      for (uint32_t k = 0; k < K; ++k) w[k] = __ldcs(reinterpret_cast<const T*>(src) + threadIdx.x + k * kAgThreads);
+    }
+    uint8_t* stage = smem + (it % kAgStages) * TB;
+    // the stage was last handed to bulk stores kAgStages tiles ago: wait until they have read it
+    if (it >= kAgStages && threadIdx.x == 0)
+      asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kAgStages - 1) : "memory");
+    __syncthreads();
+    if constexpr (G == 0) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        *reinterpret_cast<Vec*>(stage + ((uint32_t)u * kAgThreads + threadIdx.x) * kVecBytes) = v[u];
+    } else {
+#pragma unroll
+      for (uint32_t k = 0; k < K; ++k) reinterpret_cast<T*>(stage)[threadIdx.x + k * kAgThreads] = w[k];
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic-proxy writes -> bulk copies
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint64_t off = (vb + t * TV * V) * ES;
+      for (int r = 0; r < n; ++r) bulk_store(static_cast<char*>(a.dst[r]) + off, stage, TB);
+      bulk_commit();
+    }
+  }
+}
+
 // grid (CTAs per chunk, N), kAgThreads threads, kAgStages * ag_tile_bytes<kUnroll>()
 // of dynamic shared memory. The chunk's whole tiles go through shared memory and
 // bulk stores; the leftover vectors and the edge elements take plain stores.
@@ -93,36 +143,25 @@ __global__ void __launch_bounds__(kAgThreads) ag_tma_store_kernel(const __grid_c
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   constexpr uint32_t TV = (uint32_t)kAgThreads * kUnroll;  // vectors per tile
-  constexpr uint32_t TB = ag_tile_bytes<kUnroll>();
   const int n = a.nranks, c = blockIdx.y;
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
   const uint64_t nv = (ve - vb) / V;
   const uint64_t ntiles = nv / TV;
-  const void* in = a.src[c];
+  const char* in = static_cast<const char*>(a.src[c]);
   const bool in_vec = (a.compact_aligned >> c) & 1u;
 
-  uint32_t it = 0;
-  for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-    Vec v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      v[u] = ag_load<DT>(in, in_vec, (vb + (t * TV + (uint64_t)u * kAgThreads + threadIdx.x) * V) * ES, b0);
-    uint8_t* stage = smem + (it % kAgStages) * TB;
-    // the stage was last handed to bulk stores kAgStages tiles ago: wait until they have read it
-    if (it >= kAgStages && threadIdx.x == 0)
-      asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kAgStages - 1) : "memory");
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      *reinterpret_cast<Vec*>(stage + ((uint32_t)u * kAgThreads + threadIdx.x) * kVecBytes) = v[u];
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic-proxy writes -> bulk copies
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint64_t off = (vb + t * TV * V) * ES;
-      for (int r = 0; r < n; ++r) bulk_store(static_cast<char*>(a.dst[r]) + off, stage, TB);
-      bulk_commit();
+  if (ntiles > 0) {
+    if (in_vec) {
+      ag_tiles<DT, kUnroll, 0>(a, smem, in, vb, b0, ntiles);
+    } else {
+      switch (unit_bytes(in + (vb - b0) * ES)) {
+        case 16: ag_tiles<DT, kUnroll, 16>(a, smem, in, vb, b0, ntiles); break;
+        case 8: ag_tiles<DT, kUnroll, 8>(a, smem, in, vb, b0, ntiles); break;
+        case 4: ag_tiles<DT, kUnroll, 4>(a, smem, in, vb, b0, ntiles); break;
+        default: ag_tiles<DT, kUnroll, 2>(a, smem, in, vb, b0, ntiles); break;
+      }
     }
   }
 

@@ -134,6 +134,24 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
   return RA_SUCCESS;
 }
 
+// A reduce-scatter whose compact output for some chunk sits off the vector
+// grid at a 2-byte (odd-element) offset: its stores need the cooperative
+// OFFGRID kernel. Wider offsets are stored per lane in 4-16-byte units.
+bool rs_needs_offgrid(const ra::Args& a, void* const* recvbufs, int es) {
+  const int n = a.nranks;
+  const uint64_t v = (uint64_t)(ra::kVecBytes / es);
+  for (int c = 0; c < n; ++c) {
+    if ((a.compact_aligned >> c) & 1u) continue;
+    const uint64_t b0 = ra::chunk_begin(c, n, a.count), b1 = ra::chunk_begin(c + 1, n, a.count);
+    uint64_t vb = b0, ve = b0;
+    ra::vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, v, &vb, &ve);
+    if (ve == vb) continue;  // no whole vectors: element path only
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(recvbufs[c]) + (uintptr_t)((vb - b0) * (uint64_t)es);
+    if ((addr & 3u) != 0) return true;
+  }
+  return false;
+}
+
 // SMs the launch may fill: all of them, or the caller's budget (max_sms > 0)
 // when other work runs beside the collective.
 ra_status_t sm_budget(int max_sms, int* sms) {
@@ -273,11 +291,11 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
   const ra_status_t st = sm_budget(max_sms, &sms);
   if (st != RA_SUCCESS) return st;
   // resident CTAs per SM: shared memory (N slots per thread) and at most 1024 threads
-  const uint64_t smem = (uint64_t)n * ra::kOrdThreads * ra::kVecBytes;
+  const uint64_t smem = (uint64_t)n * ra::kOrdThreads * ra::kOrdVecBytes;
   uint64_t per_sm = (uint64_t)(220 * 1024) / smem;
   if (per_sm > 1024 / ra::kOrdThreads) per_sm = 1024 / ra::kOrdThreads;
   if (per_sm < 1) per_sm = 1;
-  const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
+  const uint64_t v = (uint64_t)(ra::kOrdVecBytes / elem_size(dtype));
   const uint64_t per_chunk = (a.count + n - 1) / n;
   const uint64_t work = a.vec_ok ? per_chunk / v + 1 : per_chunk;
   uint64_t gx = (work + ra::kOrdThreads - 1) / ra::kOrdThreads;
@@ -316,7 +334,11 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   if (order != RA_ORDER_RING) return run_ordered(kind, a, dtype, op, order, max_sms, stream);
   a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
   a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ra::ag_plan_for(nranks).kernel
-                                       : ra::shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0);
+                                       : ra::shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
+                                                       dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
+                                                       op == RA_MIN || op == RA_MAX);
+  if (kind == ra::KIND_REDUCE_SCATTER && a.vec_ok && rs_needs_offgrid(a, recvbufs, elem_size(dtype)))
+    a.shape = a.acc32 ? ra::SHAPE_RS_OFFGRID_M : ra::SHAPE_RS_OFFGRID;
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
   if (st != RA_SUCCESS) return st;

@@ -67,15 +67,30 @@ using ShapeM = ShapeS;
 using ShapeW = ShapeS;
 #endif
 using StepShape = Shape<256, 2, 1, 1>;  // ring-step kernels
-enum ShapeId { SHAPE_S = 0, SHAPE_N3 = 1, SHAPE_M = 2, SHAPE_W = 3, SHAPE_STEP = 5 };
+// SHAPE_RS_OFFGRID(_M): a reduce-scatter with some compact output off the
+// vector grid at a 2-byte offset, on ShapeS (ShapeM with fp32 partials).
+enum ShapeId {
+  SHAPE_S = 0,
+  SHAPE_N3 = 1,
+  SHAPE_M = 2,
+  SHAPE_W = 3,
+  SHAPE_RS_OFFGRID = 4,
+  SHAPE_STEP = 5,
+  SHAPE_RS_OFFGRID_M = 6
+};
 
-// The fused shape for a call. fp32 partials (fp16/bf16 with fp32
-// accumulation) need more registers than ShapeS leaves, so those calls take
-// ShapeM where the plain call would take ShapeS.
-inline int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false) {
-  if (reduce_scatter || nranks <= 2) return acc32 ? SHAPE_M : SHAPE_S;
+// The fused shape for a call. fp16/bf16 folds do more ALU work per byte
+// (widen, fp32 op, paired RNE conversion) and from N = 8 to 11 run best with
+// 2 CTAs/SM (98.9% at N = 8 against 93.4% with the fp32 choice). fp32
+// partials (fp16/bf16 with fp32 accumulation) fit ShapeS's 64 registers in an
+// all-reduce of sum, avg or prod (99% at N = 2), but not for min/max or in a
+// reduce-scatter, which take ShapeM; ShapeN3 cannot hold them either.
+inline int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
+                     bool minmax = false) {
+  if (reduce_scatter) return acc32 ? SHAPE_M : SHAPE_S;
+  if (nranks <= 2) return (acc32 && minmax) ? SHAPE_M : SHAPE_S;
   if (nranks == 3) return acc32 ? SHAPE_M : SHAPE_N3;
-  if (nranks <= 7) return SHAPE_M;
+  if (nranks <= 7 || (narrow && nranks < 12)) return SHAPE_M;
   return SHAPE_W;
 }
 
@@ -286,7 +301,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(
 // ---------------------------------------------------------------------------
 // reduce-scatter: chunk c's fold goes to dst[c], compact (element i -> i - b0)
 // ---------------------------------------------------------------------------
-template <int DT, int OP, bool ACC32, class SH>
+template <int DT, int OP, bool ACC32, class SH, bool OFFGRID = false>
 __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(const __grid_constant__ Args a) {
   constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
@@ -298,7 +313,16 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
   const Span sp = cta_span<SH>((ve - vb) / V);
   void* out = a.dst[c];
   const bool out_vec = (a.compact_aligned >> c) & 1u;
-  for (uint64_t j0 = sp.jbeg + threadIdx.x; j0 < sp.jend; j0 += sp.jstride) {
+  // Off the vector grid the plain kernel stores each lane's vector in 4-byte
+  // units. OFFGRID (chosen when some chunk's output is only 2-byte aligned
+  // against the grid) sends such a chunk's results out through this slice
+  // instead: a warp's 32 consecutive results, consecutive lanes on consecutive
+  // 2-byte units, so each warp store covers 64 contiguous bytes.
+  __shared__ Vec stage[OFFGRID ? kThreads : 1];
+  const uint32_t lane = threadIdx.x & 31u, wfirst = threadIdx.x & ~31u;
+  // warp-uniform trips (the warp synchronises on the off-grid path)
+  for (uint64_t jw0 = sp.jbeg + wfirst; jw0 < sp.jend; jw0 += sp.jstride) {
+    const uint64_t j0 = jw0 + lane;
     uint64_t off[kUnroll];
     bool ok[kUnroll];
 #pragma unroll
@@ -311,13 +335,24 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
     fold<DT, OP, ACC32, kUnroll, SH::kBatch>(a, c, n, off, ok, acc);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (!ok[u]) continue;
       if (out_vec) {
-        st_vec(static_cast<char*>(out) + off[u] - b0 * ES, acc[u]);
-      } else {
-        const uint64_t i = off[u] / ES - b0;
-#pragma unroll
-        for (int l = 0; l < V; ++l) st_elem<DT>(out, i + l, vec_lane<DT>(acc[u], l));
+        if (ok[u]) st_vec(static_cast<char*>(out) + off[u] - b0 * ES, acc[u]);
+      } else if constexpr (OFFGRID) {
+        const uint64_t jw = jw0 + (uint64_t)u * kThreads;  // the warp's first vector this trip
+        char* wdst = static_cast<char*>(out) + (vb + jw * V - b0) * ES;
+        if ((reinterpret_cast<uintptr_t>(wdst) & 3u) == 0) {  // the chunk allows 4-byte units
+          if (ok[u]) st_vec_units(static_cast<char*>(out) + off[u] - b0 * ES, acc[u]);
+        } else {  // 2-byte units: the warp's results go out through shared memory, lanes on consecutive units
+          const uint32_t bytes = (jw >= sp.jend ? 0u : (sp.jend - jw < 32 ? (uint32_t)(sp.jend - jw) : 32u)) * kVecBytes;
+          stage[threadIdx.x] = acc[u];
+          __syncwarp();
+          const char* sw = reinterpret_cast<const char*>(stage + wfirst);
+          for (uint32_t o = lane * 2u; o < bytes; o += 64u)
+            __stcs(reinterpret_cast<unsigned short*>(wdst + o), *reinterpret_cast<const unsigned short*>(sw + o));
+          __syncwarp();
+        }
+      } else if (ok[u]) {
+        st_vec_units(static_cast<char*>(out) + off[u] - b0 * ES, acc[u]);
       }
     }
   }
@@ -451,9 +486,9 @@ cudaError_t launch_ar(const Args& a, dim3 grid, cudaStream_t s) {
   ar_fused_kernel<DT, OP, ACC32, SH><<<grid, SH::kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
-template <int DT, int OP, bool ACC32, class SH>
+template <int DT, int OP, bool ACC32, class SH, bool OFFGRID = false>
 cudaError_t launch_rs(const Args& a, dim3 grid, cudaStream_t s) {
-  rs_fused_kernel<DT, OP, ACC32, SH><<<grid, SH::kThreads, 0, s>>>(a);
+  rs_fused_kernel<DT, OP, ACC32, SH, OFFGRID><<<grid, SH::kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 template <int DT, int OP, bool ACC32, class SH>
@@ -469,6 +504,9 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
   switch (a.shape) {
     case SHAPE_S:
       if constexpr (!ACC32) return launch_fused_shape<DT, OP, false, ShapeS>(kind, a, grid, s);
+      if constexpr (ACC32 && OP != OP_MIN && OP != OP_MAX) {
+        if (!rs) return launch_ar<DT, OP, true, ShapeS>(a, grid, s);
+      }
       break;
     case SHAPE_N3:
       if constexpr (!ACC32) {
@@ -478,6 +516,14 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
     case SHAPE_M: return launch_fused_shape<DT, OP, ACC32, ShapeM>(kind, a, grid, s);
     case SHAPE_W:
       if (!rs) return launch_ar<DT, OP, ACC32, ShapeW>(a, grid, s);
+      break;
+    case SHAPE_RS_OFFGRID:
+      if constexpr (!ACC32) {
+        if (rs) return launch_rs<DT, OP, false, ShapeS, true>(a, grid, s);
+      }
+      break;
+    case SHAPE_RS_OFFGRID_M:
+      if (rs) return launch_rs<DT, OP, ACC32, ShapeM, true>(a, grid, s);
       break;
   }
   return cudaErrorInvalidValue;
@@ -504,6 +550,8 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_N3: return shape_params_of<ShapeN3>(threads, unroll, min_blocks);
     case SHAPE_M: return shape_params_of<ShapeM>(threads, unroll, min_blocks);
     case SHAPE_W: return shape_params_of<ShapeW>(threads, unroll, min_blocks);
+    case SHAPE_RS_OFFGRID: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
+    case SHAPE_RS_OFFGRID_M: return shape_params_of<ShapeM>(threads, unroll, min_blocks);
     default: return shape_params_of<StepShape>(threads, unroll, min_blocks);
   }
 }

@@ -34,19 +34,19 @@ struct Elem {
 };
 
 // ---- scalar helpers on storage bits (held in the low bits of a uint32) ----
+// IEEE 754-2019 minimum / maximum: a NaN operand gives NaN, -0 < +0. The PTX
+// min.NaN / max.NaN instructions compute exactly this on sm_103a (checked on
+// GB300: max(-0, +0) = +0 and min = -0 in either order, NaN in either operand
+// gives the canonical NaN, subnormals kept), one instruction per hop.
 __device__ __forceinline__ float fminimum(float a, float b) {
-  if (a != a) return a;
-  if (b != b) return b;
-  if (a < b) return a;
-  if (b < a) return b;
-  return __int_as_float(__float_as_int(a) | __float_as_int(b));  // equal: -0 wins
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 __device__ __forceinline__ float fmaximum(float a, float b) {
-  if (a != a) return a;
-  if (b != b) return b;
-  if (a > b) return a;
-  if (b > a) return b;
-  return __int_as_float(__float_as_int(a) & __float_as_int(b));  // equal: +0 wins
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
 template <int DT>
@@ -74,6 +74,21 @@ __device__ __forceinline__ uint32_t minmax16(uint32_t a, uint32_t b) {
   if (IS_MAX ? (fa > fb) : (fa < fb)) return a;
   if (IS_MAX ? (fb > fa) : (fb < fa)) return b;
   return IS_MAX ? (a & b) : (a | b);  // equal values: only the sign of zero can differ
+}
+
+// The same minimum / maximum on the two 16-bit lanes of a word at once
+// (min.NaN / max.NaN on f16x2 or bf16x2: the same semantics per lane).
+template <int DT, bool IS_MAX>
+__device__ __forceinline__ uint32_t minmax16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if constexpr (DT == DT_F16) {
+    if constexpr (IS_MAX) asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else asm("min.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  } else {
+    if constexpr (IS_MAX) asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  }
+  return r;
 }
 
 // One hop on one element: `partial` (incoming) on the left, `local` on the right.
@@ -136,9 +151,7 @@ __device__ __forceinline__ uint32_t word_hop(uint32_t a, uint32_t b) {
       return *reinterpret_cast<const uint32_t*>(&h);
     }
   } else {
-    const uint32_t lo = elem_hop<DT, OP>(a & 0xffffu, b & 0xffffu);
-    const uint32_t hi = elem_hop<DT, OP>(a >> 16, b >> 16);
-    return lo | (hi << 16);
+    return minmax16x2<DT, OP == OP_MAX>(a, b);
   }
 }
 
@@ -158,32 +171,35 @@ __device__ __forceinline__ uint32_t word_avg(uint32_t v, float inv_n, int n) {
   }
 }
 
-// A vector of kVecBytes (16, or 32 with the sm_100+ 256-bit accesses), held
-// as 32-bit words: fp32/int32 lanes are words, fp16/bf16 lanes are half-words
-// (lane l in word l/2, low half first).
-constexpr int kVecWords = kVecBytes / 4;
-struct __align__(16) Vec {
-  uint32_t w[kVecWords];
+// A vector of W 32-bit words (16 or 32 bytes): fp32/int32 lanes are words,
+// fp16/bf16 lanes are half-words (lane l in word l/2, low half first). Vec is
+// the width of the fused kernels: kVecBytes (16, or 32 with the sm_100+
+// 256-bit accesses).
+template <int W>
+struct __align__(16) VecT {
+  uint32_t w[W];
 };
+constexpr int kVecWords = kVecBytes / 4;
+using Vec = VecT<kVecWords>;
 
-template <int DT, int OP>
-__device__ __forceinline__ Vec vec_hop(const Vec& a, const Vec& b) {
-  Vec r;
+template <int DT, int OP, int W>
+__device__ __forceinline__ VecT<W> vec_hop(const VecT<W>& a, const VecT<W>& b) {
+  VecT<W> r;
 #pragma unroll
-  for (int k = 0; k < kVecWords; ++k) r.w[k] = word_hop<DT, OP>(a.w[k], b.w[k]);
+  for (int k = 0; k < W; ++k) r.w[k] = word_hop<DT, OP>(a.w[k], b.w[k]);
   return r;
 }
-template <int DT>
-__device__ __forceinline__ Vec vec_avg(const Vec& v, float inv_n, int n) {
-  Vec r;
+template <int DT, int W>
+__device__ __forceinline__ VecT<W> vec_avg(const VecT<W>& v, float inv_n, int n) {
+  VecT<W> r;
 #pragma unroll
-  for (int k = 0; k < kVecWords; ++k) r.w[k] = word_avg<DT>(v.w[k], inv_n, n);
+  for (int k = 0; k < W; ++k) r.w[k] = word_avg<DT>(v.w[k], inv_n, n);
   return r;
 }
 
 // lane l of a vector, as storage bits
-template <int DT>
-__device__ __forceinline__ uint32_t vec_lane(const Vec& v, int l) {
+template <int DT, int W>
+__device__ __forceinline__ uint32_t vec_lane(const VecT<W>& v, int l) {
   if constexpr (Elem<DT>::kSize == 4) {
     return v.w[l];
   } else {
@@ -261,9 +277,11 @@ __device__ __forceinline__ VecF vecf_hop(const VecF& a, const VecF& b) {
 #define RA_ST_HINT ""
 #endif
 
-__device__ __forceinline__ Vec ld_vec(const void* p) {
-  Vec v;
-  if constexpr (kVecWords == 4) {
+template <int W>
+__device__ __forceinline__ VecT<W> ld_vec_w(const void* p) {
+  static_assert(W == 4 || W == 8, "16- or 32-byte vectors");
+  VecT<W> v;
+  if constexpr (W == 4) {
     asm volatile("ld.global" RA_LD_HINT ".v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
                  : "l"(p));
@@ -275,8 +293,11 @@ __device__ __forceinline__ Vec ld_vec(const void* p) {
   }
   return v;
 }
-__device__ __forceinline__ void st_vec(void* p, const Vec& v) {
-  if constexpr (kVecWords == 4) {
+__device__ __forceinline__ Vec ld_vec(const void* p) { return ld_vec_w<kVecWords>(p); }
+template <int W>
+__device__ __forceinline__ void st_vec(void* p, const VecT<W>& v) {
+  static_assert(W == 4 || W == 8, "16- or 32-byte vectors");
+  if constexpr (W == 4) {
     asm volatile("st.global" RA_ST_HINT ".v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
                  "r"(v.w[2]), "r"(v.w[3])
                  : "memory");
@@ -300,6 +321,57 @@ __device__ __forceinline__ void st_elem(void* base, uint64_t i, uint32_t v) {
     __stcs(reinterpret_cast<unsigned int*>(base) + i, v);
   } else {
     __stcs(reinterpret_cast<unsigned short*>(base) + i, (unsigned short)v);
+  }
+}
+
+// ---- compact buffers off the vector grid -----------------------------------
+// A compact RS output or AG input whose address phase differs from the vector
+// grid's is moved in g-byte units, g the largest power of two up to 16 that
+// divides its address. With consecutive threads on consecutive units every
+// warp access covers whole sectors; each lane storing its own vector in
+// 2-byte pieces would scatter them over 32 sectors per instruction.
+__device__ __forceinline__ uint32_t unit_bytes(const void* p) {
+  const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(p) & 15u;
+  return a == 0 ? 16u : (a & (0u - a));
+}
+// `bytes` (a multiple of 16) from 16-byte-aligned shared memory s to global g;
+// thread t of nt takes units t, t + nt, ...
+__device__ __forceinline__ void copy_out_units(char* g, const char* s, uint32_t bytes, uint32_t t, uint32_t nt) {
+  const uint32_t u = unit_bytes(g);
+  if (u == 16) {
+    for (uint32_t o = t * 16u; o < bytes; o += nt * 16u)
+      __stcs(reinterpret_cast<uint4*>(g + o), *reinterpret_cast<const uint4*>(s + o));
+  } else if (u == 8) {
+    for (uint32_t o = t * 8u; o < bytes; o += nt * 8u)
+      __stcs(reinterpret_cast<uint2*>(g + o), *reinterpret_cast<const uint2*>(s + o));
+  } else if (u == 4) {
+    for (uint32_t o = t * 4u; o < bytes; o += nt * 4u)
+      __stcs(reinterpret_cast<unsigned int*>(g + o), *reinterpret_cast<const unsigned int*>(s + o));
+  } else {
+    for (uint32_t o = t * 2u; o < bytes; o += nt * 2u)
+      __stcs(reinterpret_cast<unsigned short*>(g + o), *reinterpret_cast<const unsigned short*>(s + o));
+  }
+}
+template <uint32_t G> struct UnitT;
+template <> struct UnitT<16> { using T = uint4; };
+template <> struct UnitT<8> { using T = uint2; };
+template <> struct UnitT<4> { using T = unsigned int; };
+template <> struct UnitT<2> { using T = unsigned short; };
+// One thread's vector to global p off the vector grid: 4-byte units when p's
+// address allows (the reduce-scatter's per-lane store), else 2-byte ones. The
+// planner sends calls with 2-byte offsets to the cooperative OFFGRID kernel,
+// so the 2-byte branch is a fallback that keeps any launch correct.
+template <int W>
+__device__ __forceinline__ void st_vec_units(char* p, const VecT<W>& v) {
+  if ((reinterpret_cast<uintptr_t>(p) & 3u) == 0) {
+#pragma unroll
+    for (int k = 0; k < W; ++k) __stcs(reinterpret_cast<unsigned int*>(p) + k, v.w[k]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      __stcs(reinterpret_cast<unsigned short*>(p) + 2 * k, (unsigned short)(v.w[k] & 0xffffu));
+      __stcs(reinterpret_cast<unsigned short*>(p) + 2 * k + 1, (unsigned short)(v.w[k] >> 16));
+    }
   }
 }
 

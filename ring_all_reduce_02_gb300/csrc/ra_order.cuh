@@ -19,7 +19,15 @@
 
 namespace ra {
 
-constexpr int kOrdThreads = 2048 / kVecBytes;  // 128 threads at 16-byte vectors
+// The ordered kernel stages 16-byte vectors (the grid of the plan is laid on
+// lines of at least 32 bytes, so 16-byte vectors tile it too): with 32-byte
+// slots it measured 85-87% of the copy bandwidth against 91% with 16-byte ones.
+constexpr int kOrdVecBytes = 16;
+using OVec = VecT<kOrdVecBytes / 4>;
+#ifndef RA_ORD_THREADS
+#define RA_ORD_THREADS (2048 / 16)  // 2 KB of vectors per CTA and rank slot
+#endif
+constexpr int kOrdThreads = RA_ORD_THREADS;
 constexpr int kMaxProgSteps = RA_MAX_RANKS - 1;
 
 struct OrderArgs {
@@ -51,10 +59,10 @@ __device__ __forceinline__ uint32_t run_prog_elem(const OrderArgs& o, int pr, in
 
 // IS_RS: reduce-scatter (chunk c to dst[c], compact) instead of all-reduce.
 template <int DT, int OP, bool IS_RS>
-__global__ void __launch_bounds__(kOrdThreads, 8) ordered_kernel(const __grid_constant__ OrderArgs o) {
+__global__ void __launch_bounds__(kOrdThreads, 6) ordered_kernel(const __grid_constant__ OrderArgs o) {
   extern __shared__ __align__(128) uint8_t slots[];  // [rank][thread] vectors
-  constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
+  constexpr int V = kOrdVecBytes / ES;  // elements per staged vector
   const Args& a = o.base;
   const int n = a.nranks, c = blockIdx.y;
   const int pr = (int)((o.chunk_prog >> c) & 1u);
@@ -62,37 +70,56 @@ __global__ void __launch_bounds__(kOrdThreads, 8) ordered_kernel(const __grid_co
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
   const uint64_t nv = (ve - vb) / V;
-  Vec* my = reinterpret_cast<Vec*>(slots) + threadIdx.x;  // slot r at my[r * kOrdThreads]
+  OVec* my = reinterpret_cast<OVec*>(slots) + threadIdx.x;  // slot r at my[r * kOrdThreads]
   void* out = a.dst[c];
   const bool out_vec = !IS_RS || ((a.compact_aligned >> c) & 1u);
-  for (uint64_t j = (uint64_t)blockIdx.x * kOrdThreads + threadIdx.x; j < nv;
-       j += (uint64_t)gridDim.x * kOrdThreads) {
-    const uint64_t off = (vb + j * V) * ES;
+  // A warp stages its 32 consecutive vectors of each rank as one contiguous run of
+  // 16-byte pieces, lane l copying pieces l, l + 32, ...: every cp.async instruction
+  // covers 512 contiguous bytes. A lane's slots are thus filled by other lanes, so
+  // the warp synchronises after the copies land and before the slots are refilled.
+  constexpr uint32_t kPieces = kOrdVecBytes / 16;
+  const uint32_t lane = threadIdx.x & 31u, wbase = threadIdx.x & ~31u;
+  for (uint64_t jw = (uint64_t)blockIdx.x * kOrdThreads + wbase; jw < nv;
+       jw += (uint64_t)gridDim.x * kOrdThreads) {
+    const uint64_t j = jw + lane;
+    const uint64_t off0 = (vb + jw * V) * ES;  // the warp's first vector
     for (int r = 0; r < n; ++r) {
-      const char* g = static_cast<const char*>(a.src[r]) + off;
+      const char* g = static_cast<const char*>(a.src[r]) + off0;
+      char* sw = reinterpret_cast<char*>(reinterpret_cast<OVec*>(slots) + r * kOrdThreads + wbase);
 #pragma unroll
-      for (int h = 0; h < kVecBytes / 16; ++h)
-        cp_async_16(reinterpret_cast<char*>(my + r * kOrdThreads) + 16 * h, g + 16 * h);
+      for (uint32_t h = 0; h < kPieces; ++h) {
+        const uint32_t p = h * 32u + lane;
+        if (jw + p / kPieces < nv) cp_async_16(sw + 16u * p, g + 16u * p);
+      }
     }
     cp_async_wait_all();
-    for (int t = 0; t < o.prog_len[pr]; ++t) {
-      Vec* sa = my + o.prog[pr][t][0] * kOrdThreads;
-      const Vec* sb = my + o.prog[pr][t][1] * kOrdThreads;
-      *sa = vec_hop<DT, OP>(*sa, *sb);
-    }
-    Vec v = my[o.root[pr] * kOrdThreads];
-    if constexpr (OP == OP_AVG) v = vec_avg<DT>(v, a.inv_n, n);
-    if constexpr (IS_RS) {
-      if (out_vec) {
-        st_vec(static_cast<char*>(out) + off - b0 * ES, v);
-      } else {
-        const uint64_t i = off / ES - b0;
-#pragma unroll
-        for (int l = 0; l < V; ++l) st_elem<DT>(out, i + l, vec_lane<DT>(v, l));
+    __syncwarp();
+    if (j < nv) {
+      const uint64_t off = (vb + j * V) * ES;
+      for (int t = 0; t < o.prog_len[pr]; ++t) {
+        OVec* sa = my + o.prog[pr][t][0] * kOrdThreads;
+        const OVec* sb = my + o.prog[pr][t][1] * kOrdThreads;
+        *sa = vec_hop<DT, OP>(*sa, *sb);
       }
-    } else {
-      for (int r = 0; r < n; ++r) st_vec(static_cast<char*>(a.dst[r]) + off, v);
+      OVec v = my[o.root[pr] * kOrdThreads];
+      if constexpr (OP == OP_AVG) v = vec_avg<DT>(v, a.inv_n, n);
+      if constexpr (IS_RS) {
+        if (out_vec) st_vec(static_cast<char*>(out) + off - b0 * ES, v);
+        else my[0] = v;  // slot 0 of this lane is no longer read: it stages the result
+      } else {
+        for (int r = 0; r < n; ++r) st_vec(static_cast<char*>(a.dst[r]) + off, v);
+      }
     }
+    if constexpr (IS_RS) {
+      if (!out_vec) {  // off the vector grid: the warp writes its results in address-suited units
+        __syncwarp();
+        const uint32_t nw = nv - jw < 32 ? (uint32_t)(nv - jw) : 32u;
+        copy_out_units(static_cast<char*>(out) + (vb + jw * V - b0) * ES,
+                       reinterpret_cast<const char*>(reinterpret_cast<OVec*>(slots) + wbase), nw * kOrdVecBytes,
+                       lane, 32);
+      }
+    }
+    __syncwarp();
   }
   const uint64_t n_lo = vb - b0, total = n_lo + (b1 - ve);
   for (uint64_t k = (uint64_t)blockIdx.x * kOrdThreads + threadIdx.x; k < total;
@@ -109,7 +136,7 @@ __global__ void __launch_bounds__(kOrdThreads, 8) ordered_kernel(const __grid_co
 
 template <int DT, int OP>
 cudaError_t launch_ordered_op(bool is_rs, const OrderArgs& o, dim3 grid, cudaStream_t s) {
-  const size_t smem = (size_t)o.base.nranks * kOrdThreads * kVecBytes;
+  const size_t smem = (size_t)o.base.nranks * kOrdThreads * kOrdVecBytes;
   cudaError_t err;
   if (is_rs) {
     err = cudaFuncSetAttribute(ordered_kernel<DT, OP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
