@@ -60,11 +60,13 @@ using ShapeS = Shape<128, 8, 1, 4>;   // all-reduce nranks 1..2; every reduce-sc
 using ShapeN3 = Shape<256, 1, 4, 4>;  // all-reduce nranks 3
 using ShapeM = Shape<256, 2, 1, 4>;   // all-reduce nranks 4..7; fp32 partials where ShapeS would spill
 using ShapeW = Shape<256, 1, 2, 4>;   // all-reduce nranks >= 8
+using ShapeM3 = Shape<256, 3, 1, 4>;  // min/max at nranks 6..7, fp32 partials at nranks 3 (and min/max <= 2)
 #else  // tuning sweeps: one shape (RA_TUNE_T, _MB, _U, _B) for every rank count
 using ShapeS = Shape<RA_TUNE_T, RA_TUNE_MB, RA_TUNE_U, RA_TUNE_B>;
 using ShapeN3 = ShapeS;
 using ShapeM = ShapeS;
 using ShapeW = ShapeS;
+using ShapeM3 = ShapeS;
 #endif
 using StepShape = Shape<256, 2, 1, 1>;  // ring-step kernels
 // SHAPE_RS_OFFGRID(_M): a reduce-scatter with some compact output off the
@@ -76,21 +78,26 @@ enum ShapeId {
   SHAPE_W = 3,
   SHAPE_RS_OFFGRID = 4,
   SHAPE_STEP = 5,
-  SHAPE_RS_OFFGRID_M = 6
+  SHAPE_RS_OFFGRID_M = 6,
+  SHAPE_M3 = 7
 };
 
 // The fused shape for a call. fp16/bf16 folds do more ALU work per byte
-// (widen, fp32 op, paired RNE conversion) and from N = 8 to 11 run best with
-// 2 CTAs/SM (98.9% at N = 8 against 93.4% with the fp32 choice). fp32
-// partials (fp16/bf16 with fp32 accumulation) fit ShapeS's 64 registers in an
-// all-reduce of sum, avg or prod (99% at N = 2), but not for min/max or in a
-// reduce-scatter, which take ShapeM; ShapeN3 cannot hold them either.
+// (widen, fp32 op, paired RNE conversion) and from N = 8 to 15 run best with
+// 2 CTAs/SM (98.9% at N = 8 against 93.4% with the fp32 choice; 96% at
+// N = 12 against 91%). fp32 partials (fp16/bf16 with fp32 accumulation) fit
+// ShapeS's 64 registers in an all-reduce of sum, avg or prod (99% at N = 2),
+// not for min/max or in a reduce-scatter; ShapeN3 cannot hold them either.
+// ShapeM3 (3 CTAs/SM) serves min/max at N = 6, 7 (94-96% against 81-84% on
+// ShapeM, where avg does better), fp32 partials at N = 3 (97% against 85%) and
+// min/max fp32 partials at N <= 2 (92% against 80%).
 inline int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
                      bool minmax = false) {
   if (reduce_scatter) return acc32 ? SHAPE_M : SHAPE_S;
-  if (nranks <= 2) return (acc32 && minmax) ? SHAPE_M : SHAPE_S;
-  if (nranks == 3) return acc32 ? SHAPE_M : SHAPE_N3;
-  if (nranks <= 7 || (narrow && nranks < 12)) return SHAPE_M;
+  if (nranks <= 2) return (acc32 && minmax) ? SHAPE_M3 : SHAPE_S;
+  if (nranks == 3) return (acc32 || narrow) ? SHAPE_M3 : SHAPE_N3;
+  if (minmax && nranks >= 6 && nranks <= 7) return SHAPE_M3;
+  if (nranks <= 7 || (narrow && nranks < 16)) return SHAPE_M;
   return SHAPE_W;
 }
 
@@ -525,6 +532,9 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
     case SHAPE_RS_OFFGRID_M:
       if (rs) return launch_rs<DT, OP, ACC32, ShapeM, true>(a, grid, s);
       break;
+    case SHAPE_M3:
+      if (!rs) return launch_ar<DT, OP, ACC32, ShapeM3>(a, grid, s);
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -552,6 +562,7 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_W: return shape_params_of<ShapeW>(threads, unroll, min_blocks);
     case SHAPE_RS_OFFGRID: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
     case SHAPE_RS_OFFGRID_M: return shape_params_of<ShapeM>(threads, unroll, min_blocks);
+    case SHAPE_M3: return shape_params_of<ShapeM3>(threads, unroll, min_blocks);
     default: return shape_params_of<StepShape>(threads, unroll, min_blocks);
   }
 }
