@@ -481,6 +481,11 @@ def run_call(args):
     torch.cuda.set_device(0)
     dev = torch.cuda.current_device()
     n, length, dtype, op, _ = inputs.WORKLOADS[args.workload]
+    workload = args.workload
+    if args.case:  # an explicit case instead of a named workload: N,COUNT,DTYPE,OP
+        n_s, count_s, dtype, op = args.case.split(",")
+        n, length = int(n_s), int(count_s)
+        workload = f"case_n{n}_{dtype}_{op}_{length}"
     es = inputs.ELEM_SIZE[dtype]
     s_bytes = length * es
     tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "i32": torch.int32}[dtype]
@@ -525,7 +530,7 @@ def run_call(args):
     peak, peak_kind = measured_peaks()
     achieved = hbm_bytes / (mean_ms * 1e-3) / GB
     print(json.dumps({
-        "mode": "call", "call": name, "kernel": kernel, "workload": args.workload, "nranks": n, "count": length,
+        "mode": "call", "call": name, "kernel": kernel, "workload": workload, "nranks": n, "count": length,
         "dtype": dtype, "op": op, "steps": args.steps, "warmup": args.warmup,
         "inputs": "seeded normal(0, 1) drawn on the device",
         "l2": f"{hbm_bytes / GB:.2f} GB moved per launch vs ~0.13 GB L2",
@@ -639,6 +644,8 @@ def main():
     ap.add_argument("--overlap-tokens", type=int, default=2048)
     ap.add_argument("--call", default=None, choices=sorted(CALLS),
                     help="time one call alone on the workload (per-kernel roofline; not the headline)")
+    ap.add_argument("--case", default=None, metavar="N,COUNT,DTYPE,OP",
+                    help="with --call: this case instead of the named workload (e.g. 16,16777216,f32,sum)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -200,6 +200,10 @@ const ra_options_t kDefaultOptions = {RA_ORDER_RING, RA_ACCUM_DTYPE, 0, RA_ENGIN
 // The bulk engine: tiles of tile_vecs vectors per rank, as many stages as fit
 // in about 200 KB of shared memory (2..8), one CTA per SM on the budget.
 constexpr size_t kBulkSmemBudget = 200 * 1024;
+#ifndef RA_BULK_MAX_STAGES
+#define RA_BULK_MAX_STAGES 8
+#endif
+constexpr int kBulkMaxStages = RA_BULK_MAX_STAGES;
 
 ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* status, void* stream,
                      int withhold_first = 0, uint32_t status_stride = 0) {
@@ -209,13 +213,19 @@ ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* sta
   b.status_stride = status_stride;
   b.withhold_first = withhold_first;
   const int n = a.nranks;
-  // 4 KB per rank per stage (2 KB above 8 ranks), and at least one vector per consumer thread
-  uint32_t tv = (n <= 8 ? 4096u : 2048u) / (uint32_t)ra::kVecBytes;
+  // about 32 KB per stage: 32 KB / N per rank, between 4 and 16 KB (fewer, longer tiles when N
+  // is small, so the per-tile barrier work is spread over more bytes), and at least one vector
+  // per consumer thread
+  uint32_t tile_bytes = 32768u / (uint32_t)n;
+  if (tile_bytes < 4096u) tile_bytes = 4096u;
+  if (tile_bytes > 16384u) tile_bytes = 16384u;
+  uint32_t tv = tile_bytes / (uint32_t)ra::kVecBytes;
+  tv = tv / ra::kBulkConsumers * ra::kBulkConsumers;
   if (tv < (uint32_t)ra::kBulkConsumers) tv = ra::kBulkConsumers;
   b.tile_vecs = tv;
   const size_t stage_bytes = (size_t)n * b.tile_vecs * ra::kVecBytes;
   size_t stages = kBulkSmemBudget / stage_bytes;
-  if (stages > 8) stages = 8;
+  if (stages > (size_t)kBulkMaxStages) stages = kBulkMaxStages;
   if (stages < 2) return RA_ERR_UNSUPPORTED;
   b.stages = (uint32_t)stages;
   const size_t smem = 128 * ((2 * stages * 8 + 127) / 128) + stages * stage_bytes;

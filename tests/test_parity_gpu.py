@@ -299,6 +299,34 @@ def test_offset_views(ra, dtype):
             assert_same_bits(to_host(recvs[c].view, dtype), want[c], dtype, f"AG off {off}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", [3, 4, 6])
+def test_offgrid_compact_buffers_many_tiles(ra, dtype, n):
+    # compact RS outputs / AG inputs at every phase against the vector grid, with chunks several
+    # all-gather tiles (256 vectors) long: the unit-wise tile loads of the all-gather, the 4-byte
+    # per-lane and 2-byte cooperative reduce-scatter stores
+    es = ELEM_SIZE[dtype]
+    per_vec = ra.ra_vector_bytes() // es
+    length = n * 256 * per_vec * 3 + 13
+    xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=70 + n)
+    want, _, _ = oracle.allreduce(xs, "avg", dtype)
+    shards_want, _ = oracle.reduce_scatter(xs, "avg", dtype)
+    bounds = [oracle.chunk_range(length, n, c) for c in range(n)]
+    for off in range(per_vec):
+        sends = [Padded(length, dtype) for _ in range(n)]
+        for b, x in zip(sends, xs):
+            b.fill(x)
+        outs = [Padded(e - b, dtype, off) for b, e in bounds]
+        ra.ra_reduce_scatter([b.view for b in sends], [o.view for o in outs], "avg")
+        recvs = [Padded(length, dtype) for _ in range(n)]
+        ra.ra_allgather([o.view for o in outs], [r.view for r in recvs])
+        torch.cuda.synchronize()
+        for c in range(n):
+            assert outs[c].canaries_intact() and recvs[c].canaries_intact(), f"off {off} chunk {c}"
+            assert_same_bits(to_host(outs[c].view, dtype), shards_want[c], dtype, f"RS off {off} chunk {c}")
+            assert_same_bits(to_host(recvs[c].view, dtype), want[c], dtype, f"AG off {off} rank {c}")
+
+
 def test_fewer_elements_than_ranks(ra):
     # empty chunks: L < N (infra-guide 3.4 example: 3 elements over 4 ranks)
     for n, length in ((4, 3), (16, 5), (64, 63), (7, 1)):
