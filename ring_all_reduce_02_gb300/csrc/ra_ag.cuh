@@ -4,14 +4,15 @@
 //
 // HBM writes bound this kernel. On GB300 a pure stream of stores from the SMs
 // peaks near 6.4 TB/s (94% of the copy bandwidth) whatever the store width or
-// cache hint, against about 7.2 TB/s for reads. Two kernels:
-//  - ag_copy_kernel (ra_kernels.cuh): every thread loads vectors into
-//    registers and stores each to the N destinations;
-//  - ag_tma_store_kernel (below): the threads load a tile into shared memory
-//    and one thread hands it to the Tensor Memory Accelerator as N bulk
-//    stores (cp.async.bulk shared -> global, 8 KB contiguous per destination),
-//    double-buffered so the next tile loads while the last one is written.
-// The planner picks the kernel and the CTAs per SM from N.
+// cache hint, against about 7.2 TB/s for reads. The library's all-gather is
+// ag_tma_store_kernel (below): the threads load a tile into shared memory and
+// one thread hands it to the Tensor Memory Accelerator as N bulk stores
+// (cp.async.bulk shared -> global, 8 or 16 KB contiguous per destination),
+// double-buffered so the next tile loads while the last one is written. The
+// planner picks the tile and the CTAs per SM from N. ag_copy_kernel
+// (ra_kernels.cuh: every thread loads vectors into registers and stores each
+// to the N destinations) measured 84-91% at its best shape; it is kept for
+// comparison sweeps (RA_AG_TUNE_KERNEL=0).
 #pragma once
 
 #include "ra_bulk.cuh"

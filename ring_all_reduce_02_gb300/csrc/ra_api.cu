@@ -91,8 +91,8 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
 
   // Address phases: the N-way side must share one phase for the vector path
   // (AR: all sources and destinations; RS: the sources; AG: the destinations).
-  // The grid is laid on the largest alignment, up to 512 bytes (one warp's
-  // 16-byte accesses), at which every such buffer shares its phase.
+  // The grid is laid on the largest alignment, up to a 512-byte line, at
+  // which every such buffer shares its phase.
   const Range* wide = kind == ra::KIND_ALLGATHER ? recv : send;
   unsigned align = ra::kLineAlignMax;
   for (; align >= (unsigned)ra::kVecBytes; align /= 2) {
@@ -136,7 +136,8 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
 
 // A reduce-scatter whose compact output for some chunk sits off the vector
 // grid at a 2-byte (odd-element) offset: its stores need the cooperative
-// OFFGRID kernel. Wider offsets are stored per lane in 4-16-byte units.
+// OFFGRID kernel. Offsets of 4 bytes or more are stored per lane in 4-byte
+// units.
 bool rs_needs_offgrid(const ra::Args& a, void* const* recvbufs, int es) {
   const int n = a.nranks;
   const uint64_t v = (uint64_t)(ra::kVecBytes / es);

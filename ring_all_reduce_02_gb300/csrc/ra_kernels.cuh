@@ -15,9 +15,9 @@
 // rank order and derives the chunk's bounds once; blockIdx.x splits the
 // chunk's vectors among the row's CTAs (the shape's kUnroll vectors per thread
 // per trip, loads of up to kBatch ranks issued back to back before they are
-// folded). The at most 2(V-1) elements at the ends of each chunk, and every
-// element when the buffers do not share one address phase, go through the
-// per-element path.
+// folded). The elements of each chunk before its first line boundary and
+// after its last whole vector, and every element when the buffers do not
+// share one address phase, go through the per-element path.
 #pragma once
 
 #include <cuda_runtime.h>

@@ -1,4 +1,4 @@
-// Element and 16-byte-vector reduction ops of one ring hop, on sm_103a.
+// Element and vector reduction ops of one ring hop, on sm_103a.
 //
 // One hop combines the partial arriving from the left neighbour with the local
 // value and rounds the result to the buffer dtype (every hop of the ring is
@@ -9,8 +9,9 @@
 //              least 2p+2 significand bits for p = 11 (fp16) and p = 8 (bf16),
 //              so this equals the correctly rounded fp16/bf16 operation;
 //   int32      add / multiply modulo 2^32;
-//   min / max  IEEE 754-2019 minimum / maximum: a NaN operand gives NaN,
-//              -0 < +0; the result is one of the operands, bits unchanged.
+//   min / max  IEEE 754-2019 minimum / maximum: a NaN operand gives NaN
+//              (the canonical one on the vector path), -0 < +0; otherwise
+//              the result is one of the operands, bits unchanged.
 // avg = sum over the ring, then one multiply by inv_n = 1.0f/N (fp32) rounded
 // to the dtype (bitfern.com "AllReduce Explained": gradients summed, then
 // divided by the number of workers); int32 avg = wrapped sum / N, truncated.
