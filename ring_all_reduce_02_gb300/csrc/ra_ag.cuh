@@ -23,7 +23,10 @@ namespace ra {
 constexpr int kAgThreads = 256;
 using AgShape = Shape<kAgThreads, 2, 1, 1>;  // the register kernel
 
-constexpr uint32_t kAgStages = 2;
+#ifndef RA_AG_STAGES
+#define RA_AG_STAGES 2
+#endif
+constexpr uint32_t kAgStages = RA_AG_STAGES;  // tiles in shared memory per CTA
 
 enum AgKernel { AG_REGISTERS = 0, AG_TMA_STORE = 1 };
 constexpr int kShapeAgBase = 100;  // Args::shape of an all-gather launch: kShapeAgBase + AgKernel

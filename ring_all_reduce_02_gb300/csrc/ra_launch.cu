@@ -32,17 +32,26 @@ const SliceFn kSlices[4][5] = {RA_ROW(0), RA_ROW(1), RA_ROW(2), RA_ROW(3)};
 const OrderedSliceFn kOrderedSlices[4][5] = {RA_OROW(0), RA_OROW(1), RA_OROW(2), RA_OROW(3)};
 const BulkSliceFn kBulkSlices[4][5] = {RA_BROW(0), RA_BROW(1), RA_BROW(2), RA_BROW(3)};
 
+template <int DT, int kUnroll>
+cudaError_t launch_ag_tma(const Args& a, dim3 grid, cudaStream_t s) {
+  constexpr uint32_t smem = kAgStages * ag_tile_bytes<kUnroll>();
+  if constexpr (smem > 48 * 1024) {  // above the default limit of dynamic shared memory
+    const cudaError_t err =
+        cudaFuncSetAttribute(ag_tma_store_kernel<DT, kUnroll>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  ag_tma_store_kernel<DT, kUnroll><<<grid, kAgThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int DT>
 cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
   if (kind == KIND_ALLGATHER && a.shape == kShapeAgBase + AG_TMA_STORE) {
-    if (ag_plan_for(a.nranks).unroll == 2)
-      ag_tma_store_kernel<DT, 2><<<grid, kAgThreads, kAgStages * ag_tile_bytes<2>(), s>>>(a);
-    else
-      ag_tma_store_kernel<DT, 1><<<grid, kAgThreads, kAgStages * ag_tile_bytes<1>(), s>>>(a);
-  } else if (kind == KIND_ALLGATHER)
-    ag_copy_kernel<DT, AgShape><<<grid, AgShape::kThreads, 0, s>>>(a);
-  else
-    ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
+    if (ag_plan_for(a.nranks).unroll == 2) return launch_ag_tma<DT, 2>(a, grid, s);
+    return launch_ag_tma<DT, 1>(a, grid, s);
+  }
+  if (kind == KIND_ALLGATHER) ag_copy_kernel<DT, AgShape><<<grid, AgShape::kThreads, 0, s>>>(a);
+  else ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
