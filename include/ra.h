@@ -68,7 +68,7 @@ extern "C" {
 typedef enum {
   RA_SUCCESS = 0,
   RA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, nranks outside [1, 64], bad enum, count too big */
-  RA_ERR_UNSUPPORTED = 2, /* a dtype/op pair this build does not provide */
+  RA_ERR_UNSUPPORTED = 2, /* a dtype/op/option combination the library does not provide */
   RA_ERR_ALIAS = 3,       /* buffers overlap other than in the allowed in-place layout */
   RA_ERR_CUDA = 4,        /* the CUDA launch failed; see ra_last_cuda_error() */
   RA_ERR_SCRATCH_LIMIT = 5 /* ra_allreduce_bulk_noalloc: nranks above RA_NOALLOC_STATUS_WORDS */
@@ -254,7 +254,7 @@ int ra_last_cuda_error(void);
 ra_status_t ra_selftest_bulk_timeout(const void* const* sendbufs, void* const* recvbufs, size_t count,
                                      ra_dtype_t dtype, ra_op_t op, int nranks, int* status, void* stream);
 
-/* Bytes per vector access of this build's kernels (16 or 32): the address
+/* Bytes per vector access of the library's compiled kernels (16 or 32): the address
  * phase (address mod this) the buffers must share for the vector path. */
 int ra_vector_bytes(void);
 
