@@ -349,7 +349,8 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
                                                        dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
                                                        op == RA_MIN || op == RA_MAX);
   if (kind == ra::KIND_REDUCE_SCATTER && a.vec_ok && rs_needs_offgrid(a, recvbufs, elem_size(dtype)))
-    a.shape = a.acc32 ? ra::SHAPE_RS_OFFGRID_M : ra::SHAPE_RS_OFFGRID;
+    a.shape = a.acc32 ? ra::SHAPE_RS_OFFGRID_M
+                      : (a.shape == ra::SHAPE_S ? ra::SHAPE_RS_OFFGRID : ra::SHAPE_RS_OFFGRID_B2);
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
   if (st != RA_SUCCESS) return st;

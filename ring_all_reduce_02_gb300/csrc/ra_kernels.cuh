@@ -36,12 +36,15 @@ namespace ra {
 // flight is N loads x kUnroll vectors, so the rank count decides how many
 // threads per SM and vectors per thread keep HBM busiest; the host planner
 // picks the shape from N. Measured on GB300 with 32-byte vectors (fraction of
-// the copy bandwidth, fp32, 1 GiB over all ranks): all-reduce N <= 2: 96% with
-// 128 threads x 1 vector at 8 CTAs/SM; N = 3: 98% with 256 x 4 at 1 CTA/SM;
+// the copy bandwidth, fp32, 1 GiB over all ranks): all-reduce N <= 2: 99% with
+// 128 threads x 2 vectors at 4 CTAs/SM, loads of 2 ranks at a time (95% with
+// 128 x 1 at 8 CTAs/SM); N = 3: 98% with 256 x 4 at 1 CTA/SM;
 // N = 4..7: 95-99% with 256 x 1 at 2 CTAs/SM (the wide shape: 90-92% at
 // N = 6, 7); N >= 8: 256 x 2 at 1 CTA/SM (99.5% at N = 8, 97% at N = 12 and
-// 16). Reduce-scatter reads N values per element and writes one, and runs at
-// 98-102% with the small shape at every N.
+// 16). Reduce-scatter reads N values per element and writes one. Up to N = 3
+// loads of 2 ranks at a time suit it (128 x 1 at 8 CTAs/SM: 97-98%, max at
+// N = 3 98% against 89% with 4); from N = 4 sum/avg keep batches of 4 (96-102%)
+// and min/max take 128 x 2 with batches of 2 (96-103%, against 91-99%).
 // 0: the CTAs of a chunk interleave (grid-stride); 1: each CTA streams one
 // contiguous slab of the chunk.
 #ifndef RA_SCHEDULE
@@ -56,7 +59,11 @@ struct Shape {
   static constexpr int kBatch = BATCH;           // ranks whose loads are in flight together
 };
 #ifndef RA_TUNE_SHAPE
-using ShapeS = Shape<128, 8, 1, 4>;   // all-reduce nranks 1..2; every reduce-scatter
+using ShapeS = Shape<128, 8, 1, 4>;   // sum/avg/prod reduce-scatter nranks >= 4; fp16/bf16 sum/avg/prod
+                                      // all-reduce and fp32 partials at nranks 1..2
+using ShapeS4 = Shape<128, 4, 2, 2>;  // other all-reduces at nranks 1..2
+using ShapeRS2 = Shape<128, 8, 1, 2>; // reduce-scatter nranks 1..3
+using ShapeRS = Shape<128, 8, 2, 2>;  // min/max reduce-scatter nranks >= 4
 using ShapeN3 = Shape<256, 1, 4, 4>;  // all-reduce nranks 3
 using ShapeM = Shape<256, 2, 1, 4>;   // all-reduce nranks 4..7; fp32 partials where ShapeS would spill
 using ShapeW = Shape<256, 1, 2, 4>;   // all-reduce nranks >= 8
@@ -67,10 +74,14 @@ using ShapeN3 = ShapeS;
 using ShapeM = ShapeS;
 using ShapeW = ShapeS;
 using ShapeM3 = ShapeS;
+using ShapeS4 = ShapeS;
+using ShapeRS2 = ShapeS;
+using ShapeRS = ShapeS;
 #endif
 using StepShape = Shape<256, 2, 1, 1>;  // ring-step kernels
-// SHAPE_RS_OFFGRID(_M): a reduce-scatter with some compact output off the
-// vector grid at a 2-byte offset, on ShapeS (ShapeM with fp32 partials).
+// SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
+// vector grid at a 2-byte offset, on ShapeS, ShapeRS2 (where the plain call
+// would take loads of 2 ranks at a time) or ShapeM (fp32 partials).
 enum ShapeId {
   SHAPE_S = 0,
   SHAPE_N3 = 1,
@@ -79,7 +90,11 @@ enum ShapeId {
   SHAPE_RS_OFFGRID = 4,
   SHAPE_STEP = 5,
   SHAPE_RS_OFFGRID_M = 6,
-  SHAPE_M3 = 7
+  SHAPE_M3 = 7,
+  SHAPE_S4 = 8,
+  SHAPE_RS2 = 9,
+  SHAPE_RS = 10,
+  SHAPE_RS_OFFGRID_B2 = 11
 };
 
 // The fused shape for a call. fp16/bf16 folds do more ALU work per byte
@@ -93,8 +108,15 @@ enum ShapeId {
 // min/max fp32 partials at N <= 2 (92% against 80%).
 inline int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
                      bool minmax = false) {
-  if (reduce_scatter) return acc32 ? SHAPE_M : SHAPE_S;
-  if (nranks <= 2) return (acc32 && minmax) ? SHAPE_M3 : SHAPE_S;
+  if (reduce_scatter) {
+    if (acc32) return SHAPE_M;
+    if (nranks <= 3) return SHAPE_RS2;
+    return minmax ? SHAPE_RS : SHAPE_S;
+  }
+  if (nranks <= 2) {
+    if (acc32) return minmax ? SHAPE_M3 : SHAPE_S;
+    return (narrow && !minmax) ? SHAPE_S : SHAPE_S4;
+  }
   if (nranks == 3) return (acc32 || narrow) ? SHAPE_M3 : SHAPE_N3;
   if (minmax && nranks >= 6 && nranks <= 7) return SHAPE_M3;
   if (nranks <= 7 || (narrow && nranks < 16)) return SHAPE_M;
@@ -515,6 +537,21 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (!rs) return launch_ar<DT, OP, true, ShapeS>(a, grid, s);
       }
       break;
+    case SHAPE_S4:
+      if constexpr (!ACC32) {
+        if (!rs) return launch_ar<DT, OP, false, ShapeS4>(a, grid, s);
+      }
+      break;
+    case SHAPE_RS2:
+      if constexpr (!ACC32) {
+        if (rs) return launch_rs<DT, OP, false, ShapeRS2>(a, grid, s);
+      }
+      break;
+    case SHAPE_RS:
+      if constexpr (!ACC32) {
+        if (rs) return launch_rs<DT, OP, false, ShapeRS>(a, grid, s);
+      }
+      break;
     case SHAPE_N3:
       if constexpr (!ACC32) {
         if (!rs) return launch_ar<DT, OP, false, ShapeN3>(a, grid, s);
@@ -527,6 +564,11 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
     case SHAPE_RS_OFFGRID:
       if constexpr (!ACC32) {
         if (rs) return launch_rs<DT, OP, false, ShapeS, true>(a, grid, s);
+      }
+      break;
+    case SHAPE_RS_OFFGRID_B2:
+      if constexpr (!ACC32) {
+        if (rs) return launch_rs<DT, OP, false, ShapeRS2, true>(a, grid, s);
       }
       break;
     case SHAPE_RS_OFFGRID_M:
@@ -561,8 +603,12 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_M: return shape_params_of<ShapeM>(threads, unroll, min_blocks);
     case SHAPE_W: return shape_params_of<ShapeW>(threads, unroll, min_blocks);
     case SHAPE_RS_OFFGRID: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
+    case SHAPE_RS_OFFGRID_B2: return shape_params_of<ShapeRS2>(threads, unroll, min_blocks);
     case SHAPE_RS_OFFGRID_M: return shape_params_of<ShapeM>(threads, unroll, min_blocks);
     case SHAPE_M3: return shape_params_of<ShapeM3>(threads, unroll, min_blocks);
+    case SHAPE_S4: return shape_params_of<ShapeS4>(threads, unroll, min_blocks);
+    case SHAPE_RS2: return shape_params_of<ShapeRS2>(threads, unroll, min_blocks);
+    case SHAPE_RS: return shape_params_of<ShapeRS>(threads, unroll, min_blocks);
     default: return shape_params_of<StepShape>(threads, unroll, min_blocks);
   }
 }
