@@ -371,6 +371,64 @@ def sample_indices(length, n, k=1 << 17, seed=0):
     return np.unique(np.concatenate(idx)).astype(np.int64)
 
 
+def test_more_than_2_pow_32_elements(ra):
+    # L = 2^32 + 1,000,003 bf16 per rank: element indices and byte offsets past 32 bits in every
+    # kernel the call reaches (all-reduce on both engines, reduce-scatter, all-gather). Inputs
+    # are drawn on the device; the oracle gets them at the sampled indices only, in host arrays
+    # that are otherwise untouched zero pages.
+    n, length, dtype = 2, (1 << 32) + 1_000_003, "bf16"
+    need = 5 * n * length * 2 + (1 << 30)
+    if torch.cuda.mem_get_info()[0] < need:
+        pytest.skip("not enough free device memory")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    sends = []
+    for _ in range(n):
+        x = torch.empty(length, dtype=torch.bfloat16, device="cuda")
+        step = 1 << 28
+        for a in range(0, length, step):
+            b = min(length, a + step)
+            x[a:b] = torch.randn(b - a, generator=g, device="cuda").to(torch.bfloat16)
+        sends.append(x)
+    recvs = [torch.empty_like(x) for x in sends]
+    ra.ra_allreduce(sends, recvs, "sum")
+    torch.cuda.synchronize()
+    assert torch.equal(recvs[0].view(torch.int16), recvs[1].view(torch.int16))
+
+    idx = sample_indices(length, n, k=1 << 16)
+    near = np.concatenate([np.arange((1 << 31) - 8, (1 << 31) + 8), np.arange((1 << 32) - 8, (1 << 32) + 8)])
+    idx = np.unique(np.concatenate([idx, near])).astype(np.int64)
+    idx_dev = torch.from_numpy(idx).cuda()
+    xs = []
+    for x in sends:
+        h = np.zeros(length, dtype=np.uint16)  # zero pages, touched only at the samples
+        h[idx] = x[idx_dev].view(torch.int16).cpu().numpy().view(np.uint16)
+        xs.append(h)
+    want = oracle.fold_at(xs, "sum", dtype, idx)
+    assert_same_bits(to_host(recvs[0][idx_dev], dtype), want, dtype, "AR sampled past 2^32")
+
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bulk = [torch.empty_like(x) for x in sends]
+    ra.ra_allreduce_ex(sends, bulk, "sum", engine="bulk", status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(bulk[0].view(torch.int16), recvs[0].view(torch.int16)), "bulk engine differs"
+    del bulk
+
+    bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+    shards = [torch.empty(e - b, dtype=torch.bfloat16, device="cuda") for b, e in bounds]
+    ra.ra_reduce_scatter(sends, shards, "sum")
+    torch.cuda.synchronize()
+    for c, (b, e) in enumerate(bounds):
+        assert torch.equal(shards[c].view(torch.int16), recvs[0][b:e].view(torch.int16)), f"RS chunk {c}"
+    del sends
+    gathered = [torch.empty(length, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    ra.ra_allgather(shards, gathered)
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert torch.equal(gathered[r].view(torch.int16), recvs[0].view(torch.int16)), f"AG rank {r}"
+
+
 def check_full_size(ra, n, length, dtype, op, dist):
     need_gb = 2.5 * n * length * ELEM_SIZE[dtype] / 2**30
     if _host_ram_gb() < need_gb + 4:
