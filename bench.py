@@ -469,6 +469,9 @@ CALLS = {  # name: (kernel, algorithmic bytes per launch as a multiple of S, the
     "allreduce_fp32acc": ("ar_fused_kernel (fp32 partials)", lambda n: 2 * n),
     "allreduce_tree": ("ordered_kernel", lambda n: 2 * n),
     "allreduce_rabenseifner": ("ordered_kernel", lambda n: 2 * n),
+    # the literal schedule: per reduce-scatter step 3 S (read the incoming partial and the own
+    # chunk, write the sum), per all-gather step 2 S, over N-1 steps each
+    "allreduce_ringsteps": ("ring_rs_step_kernel + ring_ag_step_kernel", lambda n: 5 * (n - 1)),
 }
 
 
@@ -506,6 +509,7 @@ def run_call(args):
         "allreduce_fp32acc": lambda: ra.ra_allreduce_ex(sends, recvs, op, accum="fp32", stream=stream),
         "allreduce_tree": lambda: ra.ra_allreduce_ex(sends, recvs, op, order="tree", stream=stream),
         "allreduce_rabenseifner": lambda: ra.ra_allreduce_ex(sends, recvs, op, order="rabenseifner", stream=stream),
+        "allreduce_ringsteps": lambda: ra.ra_allreduce_ringsteps(sends, recvs, op, stream=stream),
     }[name]
     kernel, mult = CALLS[name]
     hbm_bytes = mult(n) * s_bytes

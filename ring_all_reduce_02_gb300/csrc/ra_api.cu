@@ -13,6 +13,7 @@
 #include "ra_bulk.cuh"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
+#include "ra_steps.cuh"
 
 namespace ra {
 cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid, cudaStream_t s);
@@ -44,6 +45,33 @@ struct Range {
 };
 bool overlaps(const Range& a, const Range& b) {
   return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+// ---- launch shapes of the fused kernels ------------------------------------
+// The fused shape for a call. fp16/bf16 folds do more ALU work per byte
+// (widen, fp32 op, paired RNE conversion) and from N = 8 to 15 run best with
+// 2 CTAs/SM (98.9% at N = 8 against 93.4% with the fp32 choice; 96% at
+// N = 12 against 91%). fp32 partials (fp16/bf16 with fp32 accumulation) fit
+// ShapeS's 64 registers in an all-reduce of sum, avg or prod (99% at N = 2),
+// not for min/max or in a reduce-scatter; ShapeN3 cannot hold them either.
+// ShapeM3 (3 CTAs/SM) serves min/max at N = 6, 7 (94-96% against 81-84% on
+// ShapeM, where avg does better), fp32 partials at N = 3 (97% against 85%) and
+// min/max fp32 partials at N <= 2 (92% against 80%).
+int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
+                     bool minmax = false) {
+  if (reduce_scatter) {
+    if (acc32) return ra::SHAPE_M;
+    if (nranks <= 3) return ra::SHAPE_RS2;
+    return minmax ? ra::SHAPE_RS : ra::SHAPE_S;
+  }
+  if (nranks <= 2) {
+    if (acc32) return minmax ? ra::SHAPE_M3 : ra::SHAPE_S;
+    return (narrow && !minmax) ? ra::SHAPE_S : ra::SHAPE_S4;
+  }
+  if (nranks == 3) return (acc32 || narrow) ? ra::SHAPE_M3 : ra::SHAPE_N3;
+  if (minmax && nranks >= 6 && nranks <= 7) return ra::SHAPE_M3;
+  if (nranks <= 7 || (narrow && nranks < 16)) return ra::SHAPE_M;
+  return ra::SHAPE_W;
 }
 
 // Checks shared by the three collectives; on success fills the kernel args.
@@ -130,7 +158,7 @@ ra_status_t prepare(int kind, const void* const* sendbufs, void* const* recvbufs
   a->inv_n = 1.0f / (float)nranks;
   a->step = 0;
   a->acc32 = 0;
-  a->shape = ra::shape_for(nranks);
+  a->shape = shape_for(nranks);
   return RA_SUCCESS;
 }
 
@@ -173,6 +201,8 @@ ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3*
     const ra::AgPlan p = ra::ag_plan_for(a.nranks);
     threads = ra::kAgThreads, min_blocks = p.blocks_per_sm;
     per_thread = p.kernel == ra::AG_TMA_STORE ? p.unroll : ra::AgShape::kUnroll;
+  } else if (shape == ra::SHAPE_STEP) {
+    threads = ra::StepShape::kThreads, per_thread = ra::StepShape::kUnroll, min_blocks = ra::StepShape::kMinBlocks;
   } else {
     ra::shape_params(shape, &threads, &per_thread, &min_blocks);
   }
@@ -345,7 +375,7 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   if (order != RA_ORDER_RING) return run_ordered(kind, a, dtype, op, order, max_sms, stream);
   a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
   a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ra::ag_plan_for(nranks).kernel
-                                       : ra::shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
+                                       : shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
                                                        dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
                                                        op == RA_MIN || op == RA_MAX);
   if (kind == ra::KIND_REDUCE_SCATTER && a.vec_ok && rs_needs_offgrid(a, recvbufs, elem_size(dtype)))
@@ -366,7 +396,7 @@ ra_status_t run_ringsteps(const void* const* sendbufs, void* const* recvbufs, si
   if (nsteps < 0 || nsteps > total) nsteps = total;
   dim3 grid;
   if (nranks == 1) {  // no ring steps: the result is the (avg-scaled) copy
-    a.shape = ra::shape_for(1);
+    a.shape = shape_for(1);
     st = grid_for(a, dtype, a.shape, 0, &grid);
     return st != RA_SUCCESS ? st : launch(ra::KIND_ALLREDUCE, dtype, op, a, grid, stream);
   }

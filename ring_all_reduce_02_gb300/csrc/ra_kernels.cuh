@@ -78,7 +78,6 @@ using ShapeS4 = ShapeS;
 using ShapeRS2 = ShapeS;
 using ShapeRS = ShapeS;
 #endif
-using StepShape = Shape<256, 2, 1, 1>;  // ring-step kernels
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
 // vector grid at a 2-byte offset, on ShapeS, ShapeRS2 (where the plain call
 // would take loads of 2 ranks at a time) or ShapeM (fp32 partials).
@@ -96,32 +95,6 @@ enum ShapeId {
   SHAPE_RS = 10,
   SHAPE_RS_OFFGRID_B2 = 11
 };
-
-// The fused shape for a call. fp16/bf16 folds do more ALU work per byte
-// (widen, fp32 op, paired RNE conversion) and from N = 8 to 15 run best with
-// 2 CTAs/SM (98.9% at N = 8 against 93.4% with the fp32 choice; 96% at
-// N = 12 against 91%). fp32 partials (fp16/bf16 with fp32 accumulation) fit
-// ShapeS's 64 registers in an all-reduce of sum, avg or prod (99% at N = 2),
-// not for min/max or in a reduce-scatter; ShapeN3 cannot hold them either.
-// ShapeM3 (3 CTAs/SM) serves min/max at N = 6, 7 (94-96% against 81-84% on
-// ShapeM, where avg does better), fp32 partials at N = 3 (97% against 85%) and
-// min/max fp32 partials at N <= 2 (92% against 80%).
-inline int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
-                     bool minmax = false) {
-  if (reduce_scatter) {
-    if (acc32) return SHAPE_M;
-    if (nranks <= 3) return SHAPE_RS2;
-    return minmax ? SHAPE_RS : SHAPE_S;
-  }
-  if (nranks <= 2) {
-    if (acc32) return minmax ? SHAPE_M3 : SHAPE_S;
-    return (narrow && !minmax) ? SHAPE_S : SHAPE_S4;
-  }
-  if (nranks == 3) return (acc32 || narrow) ? SHAPE_M3 : SHAPE_N3;
-  if (minmax && nranks >= 6 && nranks <= 7) return SHAPE_M3;
-  if (nranks <= 7 || (narrow && nranks < 16)) return SHAPE_M;
-  return SHAPE_W;
-}
 
 enum Kind {
   KIND_ALLREDUCE = 0,       // fused: one launch per call
@@ -443,71 +416,6 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ag_copy_kernel(c
 }
 
 // ---------------------------------------------------------------------------
-// The literal schedule, one launch per ring step (for checking and measuring
-// the fused kernels against it). blockIdx.y = rank r.
-//
-// reduce-scatter step s: rank r receives chunk C = (r - s - 1) mod N from rank
-// r-1 and combines it with its own copy: dst[r][C] = hop(in, src[r][C]), where
-// `in` is rank r-1's partial of C from step s-1 (dst[r-1][C]) or, at s = 0,
-// its input (src[r-1][C]). Each chunk of rank r is touched once in this phase,
-// so its own operand is still its input, read from src[r]; in place
-// (dst == src) this is the same memory. At s = N-2 rank r finishes chunk
-// (r+1) mod N and applies the avg epilogue to it.
-// all-gather step s: dst[r][C] = dst[r-1][C] with C = (r - s) mod N.
-// ---------------------------------------------------------------------------
-template <int DT, int OP>
-__global__ void __launch_bounds__(StepShape::kThreads, StepShape::kMinBlocks)
-    ring_rs_step_kernel(const __grid_constant__ Args a) {
-  constexpr int kThreads = StepShape::kThreads;
-  constexpr int V = Elem<DT>::kPerVec;
-  constexpr int ES = Elem<DT>::kSize;
-  const int n = a.nranks, r = blockIdx.y, s = a.step;
-  const int prev = r == 0 ? n - 1 : r - 1;
-  const int cc = ((r - s - 1) % n + n) % n;
-  const void* in = s == 0 ? a.src[prev] : a.dst[prev];
-  const void* own = a.src[r];
-  void* out = a.dst[r];
-  const bool finish = (OP == OP_AVG) && (s == n - 2);
-  const uint64_t b0 = chunk_begin(cc, n, a.count), b1 = chunk_begin(cc + 1, n, a.count);
-  uint64_t vb = b0, ve = b0;
-  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
-  const uint64_t nv = (ve - vb) / V;
-  for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < nv; j += (uint64_t)gridDim.x * kThreads) {
-    const uint64_t off = (vb + j * V) * ES;
-    Vec v = vec_hop<DT, OP>(ld_vec(static_cast<const char*>(in) + off), ld_vec(static_cast<const char*>(own) + off));
-    if (finish) v = vec_avg<DT>(v, a.inv_n, n);
-    st_vec(static_cast<char*>(out) + off, v);
-  }
-  for_each_edge_elem<kThreads>(b0, vb, ve, b1, [&](uint64_t i) {
-    uint32_t v = elem_hop<DT, OP>(ld_elem<DT>(in, i), ld_elem<DT>(own, i));
-    if (finish) v = elem_avg<DT>(v, a.inv_n, n);
-    st_elem<DT>(out, i, v);
-  });
-}
-
-template <int DT>
-__global__ void __launch_bounds__(StepShape::kThreads, StepShape::kMinBlocks)
-    ring_ag_step_kernel(const __grid_constant__ Args a) {
-  constexpr int kThreads = StepShape::kThreads;
-  constexpr int V = Elem<DT>::kPerVec;
-  constexpr int ES = Elem<DT>::kSize;
-  const int n = a.nranks, r = blockIdx.y, s = a.step;
-  const int prev = r == 0 ? n - 1 : r - 1;
-  const int cc = ((r - s) % n + n) % n;
-  const void* in = a.dst[prev];
-  void* out = a.dst[r];
-  const uint64_t b0 = chunk_begin(cc, n, a.count), b1 = chunk_begin(cc + 1, n, a.count);
-  uint64_t vb = b0, ve = b0;
-  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
-  const uint64_t nv = (ve - vb) / V;
-  for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < nv; j += (uint64_t)gridDim.x * kThreads) {
-    const uint64_t off = (vb + j * V) * ES;
-    st_vec(static_cast<char*>(out) + off, ld_vec(static_cast<const char*>(in) + off));
-  }
-  for_each_edge_elem<kThreads>(b0, vb, ve, b1, [&](uint64_t i) { st_elem<DT>(out, i, ld_elem<DT>(in, i)); });
-}
-
-// ---------------------------------------------------------------------------
 // host-side launch for one dtype (instantiated once per dtype translation unit)
 // ---------------------------------------------------------------------------
 template <int DT, int OP, bool ACC32, class SH>
@@ -581,12 +489,9 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
+// The fused all-reduce / reduce-scatter of one (dtype, op) pair.
 template <int DT, int OP>
 cudaError_t launch_op(int kind, const Args& a, dim3 grid, cudaStream_t s) {
-  if (kind == KIND_RING_RS_STEP) {
-    ring_rs_step_kernel<DT, OP><<<grid, StepShape::kThreads, 0, s>>>(a);
-    return cudaGetLastError();
-  }
   constexpr bool kNarrow = DT == DT_F16 || DT == DT_BF16;
   if (kNarrow && a.acc32) return launch_fused<DT, OP, kNarrow>(kind, a, grid, s);
   return launch_fused<DT, OP, false>(kind, a, grid, s);
@@ -609,7 +514,7 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_S4: return shape_params_of<ShapeS4>(threads, unroll, min_blocks);
     case SHAPE_RS2: return shape_params_of<ShapeRS2>(threads, unroll, min_blocks);
     case SHAPE_RS: return shape_params_of<ShapeRS>(threads, unroll, min_blocks);
-    default: return shape_params_of<StepShape>(threads, unroll, min_blocks);
+    default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
   }
 }
 

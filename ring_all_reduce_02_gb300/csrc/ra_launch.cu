@@ -4,6 +4,7 @@
 #include "ra_bulk.cuh"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
+#include "ra_steps.cuh"
 
 namespace ra {
 
@@ -50,8 +51,8 @@ cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
     if (ag_plan_for(a.nranks).unroll == 2) return launch_ag_tma<DT, 2>(a, grid, s);
     return launch_ag_tma<DT, 1>(a, grid, s);
   }
-  if (kind == KIND_ALLGATHER) ag_copy_kernel<DT, AgShape><<<grid, AgShape::kThreads, 0, s>>>(a);
-  else ring_ag_step_kernel<DT><<<grid, StepShape::kThreads, 0, s>>>(a);
+  if (kind == KIND_RING_AG_STEP) return launch_ring_ag_step<DT>(a, grid, s);
+  ag_copy_kernel<DT, AgShape><<<grid, AgShape::kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -4,6 +4,7 @@
 #include "ra_bulk.cuh"
 #include "ra_kernels.cuh"
 #include "ra_order.cuh"
+#include "ra_steps.cuh"
 
 #if !defined(RA_SLICE_DT) || !defined(RA_SLICE_OP)
 #error "compile with -DRA_SLICE_DT=<dtype id> -DRA_SLICE_OP=<op id>"
@@ -14,6 +15,7 @@
 
 namespace ra {
 cudaError_t RA_CAT3(launch_slice, RA_SLICE_DT, RA_SLICE_OP)(int kind, const Args& a, dim3 grid, cudaStream_t s) {
+  if (kind == KIND_RING_RS_STEP) return launch_ring_rs_step<RA_SLICE_DT, RA_SLICE_OP>(a, grid, s);
   return launch_op<RA_SLICE_DT, RA_SLICE_OP>(kind, a, grid, s);
 }
 cudaError_t RA_CAT3(launch_ordered_slice, RA_SLICE_DT, RA_SLICE_OP)(bool is_rs, const OrderArgs& o, dim3 grid,
