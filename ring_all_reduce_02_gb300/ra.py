@@ -281,8 +281,10 @@ def ra_chunk_range(count: int, nranks: int, c: int) -> tuple[int, int]:
     return b.value, e.value
 
 
-def ra_plan_chunk(count: int, nranks: int, c: int, elem_size: int, phase_bytes: int, align_bytes: int = 16):
-    """(begin, end, vec_begin, vec_end) of chunk c: which part takes the vector path."""
+def ra_plan_chunk(count: int, nranks: int, c: int, elem_size: int, phase_bytes: int, align_bytes: int = 0):
+    """(begin, end, vec_begin, vec_end) of chunk c: which part takes the vector path. ``align_bytes``
+    is the grid's alignment (a power of two from ra_vector_bytes() to 512; 0: ra_vector_bytes())."""
+    align_bytes = align_bytes or lib().ra_vector_bytes()
     out = [ctypes.c_size_t() for _ in range(4)]
     st = lib().ra_plan_chunk(count, nranks, c, elem_size, align_bytes, phase_bytes, *[ctypes.byref(o) for o in out])
     if st:
