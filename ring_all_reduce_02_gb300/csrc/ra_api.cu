@@ -230,7 +230,10 @@ const ra_options_t kDefaultOptions = {RA_ORDER_RING, RA_ACCUM_DTYPE, 0, RA_ENGIN
 
 // The bulk engine: tiles of tile_vecs vectors per rank, as many stages as fit
 // in about 200 KB of shared memory (2..8), one CTA per SM on the budget.
-constexpr size_t kBulkSmemBudget = 200 * 1024;
+#ifndef RA_BULK_SMEM_KB
+#define RA_BULK_SMEM_KB 200
+#endif
+constexpr size_t kBulkSmemBudget = (size_t)RA_BULK_SMEM_KB * 1024;
 #ifndef RA_BULK_MAX_STAGES
 #define RA_BULK_MAX_STAGES 8
 #endif
