@@ -56,7 +56,9 @@ bool overlaps(const Range& a, const Range& b) {
 // not for min/max or in a reduce-scatter; ShapeN3 cannot hold them either.
 // ShapeM3 (3 CTAs/SM) serves min/max at N = 6, 7 (94-96% against 81-84% on
 // ShapeM, where avg does better), fp32 partials at N = 3 (97% against 85%) and
-// min/max fp32 partials at N <= 2 (92% against 80%).
+// min/max fp32 partials at N <= 2 (92% against 80%). fp16/bf16 sum/avg/prod at
+// N = 6 load all six ranks at once (ShapeMB8: 95-96% against 92-93% with
+// batches of 4 and 2); at N = 4, 5, 7 and 8 batches of 8 measured lower.
 int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
                      bool minmax = false) {
   if (reduce_scatter) {
@@ -70,6 +72,7 @@ int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool 
   }
   if (nranks == 3) return (acc32 || narrow) ? ra::SHAPE_M3 : ra::SHAPE_N3;
   if (minmax && nranks >= 6 && nranks <= 7) return ra::SHAPE_M3;
+  if (narrow && !acc32 && nranks == 6) return ra::SHAPE_MB8;
   if (nranks <= 7 || (narrow && nranks < 16)) return ra::SHAPE_M;
   return ra::SHAPE_W;
 }
