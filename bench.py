@@ -573,7 +573,10 @@ def run_overlap(args):
     gy = torch.randn(tokens, 1024, device="cuda", generator=g).to(torch.bfloat16)
     xs = [torch.randn(max(1, c // 1024), tokens, device="cuda", generator=g).to(torch.bfloat16) for _, c in plan]
     outs = [torch.empty(x.shape[0], 1024, device="cuda", dtype=torch.bfloat16) for x in xs]
-    cs, ms = torch.cuda.Stream(), torch.cuda.Stream()
+    cs, ms_normal = torch.cuda.Stream(), torch.cuda.Stream()
+    # a high-priority communication stream: its CTAs are scheduled ahead of queued GEMM CTAs
+    lo, hi = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, -1)
+    ms_high = torch.cuda.Stream(priority=hi)
     main = torch.cuda.current_stream()
 
     def compute(events=None):
@@ -602,12 +605,12 @@ def run_overlap(args):
 
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
-    def comm_only(max_sms, engine):
+    def comm_only(max_sms, engine, ms):
         ms.wait_stream(main)
         ra.ra_allreduce_buckets(sends, recvs, plan, op, max_sms=max_sms, engine=engine, status=status, stream=ms)
         main.wait_stream(ms)
 
-    def overlapped(max_sms, engine):
+    def overlapped(max_sms, engine, ms):
         events = [torch.cuda.Event() for _ in plan]
         cs.wait_stream(main)
         ms.wait_stream(main)
@@ -621,11 +624,15 @@ def run_overlap(args):
     c_ms = timed(compute_only)
     flops = sum(2 * c * tokens for _, c in plan)
     s_bytes = length * 2
-    for engine, max_sms in [("registers", m) for m in (0, 76, 38, 16, 8)] + [("bulk", m) for m in (0, 76, 38, 16, 8)]:
-        a_ms = timed(lambda: comm_only(max_sms, engine))
-        t_ms = timed(lambda: overlapped(max_sms, engine))
+    runs = [(e, m, "normal") for e in ("registers", "bulk") for m in (0, 76, 38, 16, 8)]
+    runs += [(e, m, "high") for e in ("registers", "bulk") for m in (0, 76)]
+    for engine, max_sms, prio in runs:
+        ms = ms_high if prio == "high" else ms_normal
+        a_ms = timed(lambda: comm_only(max_sms, engine, ms))
+        t_ms = timed(lambda: overlapped(max_sms, engine, ms))
         rec = {"mode": "overlap", "workload": "ar_n8_bf16_avg_gpt2m", "buckets": len(plan),
                "bucket_cap_bytes": 25 * 1000 * 1000, "tokens": tokens, "engine": engine, "max_sms": max_sms,
+               "comm_stream_priority": prio,
                "compute_ms": round(c_ms, 3), "compute_tflops": round(flops / (c_ms * 1e-3) / 1e12, 1),
                "allreduce_ms": round(a_ms, 3), "allreduce_algbw_GBps": round(s_bytes / (a_ms * 1e-3) / GB, 1),
                "overlapped_ms": round(t_ms, 3), "exposed_comm_ms": round(t_ms - c_ms, 3),
