@@ -48,19 +48,23 @@ bool overlaps(const Range& a, const Range& b) {
 }
 
 // ---- launch shapes of the fused kernels ------------------------------------
-// The fused shape for a call. fp16/bf16 folds do more ALU work per byte
-// (widen, fp32 op, paired RNE conversion) and from N = 8 to 15 run best with
-// 2 CTAs/SM (98.9% at N = 8 against 93.4% with the fp32 choice; 96% at
-// N = 12 against 91%). fp32 partials (fp16/bf16 with fp32 accumulation) fit
-// ShapeS's 64 registers in an all-reduce of sum, avg or prod (99% at N = 2),
-// not for min/max or in a reduce-scatter; ShapeN3 cannot hold them either.
-// ShapeM3 (3 CTAs/SM) serves min/max at N = 6, 7 (94-96% against 81-84% on
-// ShapeM, where avg does better), fp32 partials at N = 3 (97% against 85%) and
-// min/max fp32 partials at N <= 2 (92% against 80%). fp16/bf16 sum/avg/prod at
-// N = 6 load all six ranks at once (ShapeMB8: 95-96% against 92-93% with
-// batches of 4 and 2); at N = 4, 5, 7 and 8 batches of 8 measured lower.
+// The fused shape for a call, from sweeps on GB300 (fraction of the copy
+// bandwidth, 1 GiB over all ranks; the shapes themselves are in ra_kernels.cuh):
+//  - reduce-scatter: loads of 2 ranks at a time up to N = 3 (ShapeRS2) and for
+//    min/max (ShapeRS), of 4 for sum/avg/prod from N = 4 (ShapeS); fp32
+//    partials on ShapeM;
+//  - all-reduce N <= 2: ShapeS4 (99%), except fp16/bf16 sum/avg/prod and fp32
+//    partials, which keep ShapeS (98.5-99%); min/max fp32 partials, which do
+//    not fit ShapeS's 64 registers, take ShapeM3 (92% against 80%);
+//  - N = 3: ShapeN3 for fp32/int32, ShapeM3 for fp16/bf16 and for fp32
+//    partials, which ShapeN3 cannot hold (97% against 85%);
+//  - min/max at N = 6, 7: ShapeM3 (94-96% against 81-84% on ShapeM);
+//  - fp16/bf16 sum/avg/prod at N = 6: all six ranks' loads at once (ShapeMB8,
+//    95-96% against 92-93%);
+//  - otherwise ShapeM up to N = 7 and, for fp16/bf16 (more ALU work per byte),
+//    up to N = 15 (98.9% at N = 8 against 93.4%); ShapeW from N = 8.
 int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
-                     bool minmax = false) {
+              bool minmax = false) {
   if (reduce_scatter) {
     if (acc32) return ra::SHAPE_M;
     if (nranks <= 3) return ra::SHAPE_RS2;
@@ -382,8 +386,8 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
   a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ra::ag_plan_for(nranks).kernel
                                        : shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
-                                                       dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
-                                                       op == RA_MIN || op == RA_MAX);
+                                                   dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
+                                                   op == RA_MIN || op == RA_MAX);
   if (kind == ra::KIND_REDUCE_SCATTER && a.vec_ok && rs_needs_offgrid(a, recvbufs, elem_size(dtype)))
     a.shape = a.acc32 ? ra::SHAPE_RS_OFFGRID_M
                       : (a.shape == ra::SHAPE_S ? ra::SHAPE_RS_OFFGRID : ra::SHAPE_RS_OFFGRID_B2);
