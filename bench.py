@@ -384,6 +384,9 @@ def run_sweep(args):
     peak, peak_kind = measured_peaks()
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     flush = torch.empty(int(2 * l2), dtype=torch.uint8, device="cuda")
+    # read after the flush to write its dirty lines back: the "clean" timing starts from an L2
+    # that holds only clean lines of unrelated data
+    evict = torch.ones(int(2 * l2) // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     out = open(args.sweep, "w")
     for (n, length, dtype, op, dist_spec) in inputs.size_sweep():
@@ -407,25 +410,36 @@ def run_sweep(args):
             for _ in range(5):
                 fn()
             reps = 20
-            times = []
-            for _ in range(reps):
-                if not resident:
-                    flush.zero_()
-                # keep the GPU busy until the launch and both events are queued, so that the
-                # interval holds the kernel alone and none of the host's call overhead
-                torch.cuda._sleep(200_000)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                fn()
-                b.record(stream)
-                torch.cuda.synchronize()
-                times.append(a.elapsed_time(b) * 1e-3)
+
+            def timed_reps(clean):
+                times = []
+                for _ in range(reps):
+                    if not resident:
+                        flush.zero_()
+                        if clean:
+                            torch.amax(evict)
+                    # keep the GPU busy until the launch and both events are queued, so that the
+                    # interval holds the kernel alone and none of the host's call overhead
+                    torch.cuda._sleep(200_000)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    times.append(a.elapsed_time(b) * 1e-3)
+                return times
+
+            times = timed_reps(False)
             rec = {"call": name, "nranks": n, "bytes_per_rank": s_bytes, "count": length,
                    "median_us": round(1e6 * statistics.median(times), 3), "min_us": round(1e6 * min(times), 3),
                    "algbw_GBps": round(s_bytes / statistics.median(times) / GB, 3),
                    "hbm_GBps": round(hbm_bytes / statistics.median(times) / GB, 1),
                    "hbm_frac": None if resident else round(hbm_bytes / statistics.median(times) / GB / peak, 4),
                    "l2_resident": resident, "peak": f"{peak} ({peak_kind})"}
+            if not resident:
+                clean = statistics.median(timed_reps(True))
+                rec["clean_median_us"] = round(1e6 * clean, 3)
+                rec["clean_hbm_frac"] = round(hbm_bytes / clean / GB / peak, 4)
             if resident:
                 # warm, back-to-back launches captured in one CUDA graph: launch cost amortised
                 gs = torch.cuda.Stream()

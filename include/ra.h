@@ -35,7 +35,11 @@
  *  - The library allocates no device memory and keeps no state between
  *    calls; calls are reentrant. Work is enqueued on `stream` (a
  *    cudaStream_t; NULL = the legacy default stream) and the call returns
- *    without waiting.
+ *    without waiting. The collective kernels are programmatic dependent
+ *    launches: their CTAs may be placed on the GPU while the previous kernel
+ *    on `stream` is finishing, but no thread reads or writes memory before
+ *    that kernel has completed, so the stream's order holds as for any
+ *    launch (a graph captured from the stream records programmatic edges).
  *  - Arguments are checked on the host before any launch; on any error
  *    nothing is enqueued. Every pointer must be aligned to the element size;
  *    a pointer to a zero-length buffer may be NULL. Any other alignment is

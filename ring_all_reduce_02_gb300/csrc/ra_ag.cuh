@@ -143,6 +143,7 @@ __device__ __forceinline__ void ag_tiles(const Args& a, uint8_t* smem, const cha
 // bulk stores; the leftover vectors and the edge elements take plain stores.
 template <int DT, int kUnroll>
 __global__ void __launch_bounds__(kAgThreads) ag_tma_store_kernel(const __grid_constant__ Args a) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;

@@ -50,9 +50,12 @@ bool overlaps(const Range& a, const Range& b) {
 // ---- launch shapes of the fused kernels ------------------------------------
 // The fused shape for a call, from sweeps on GB300 (fraction of the copy
 // bandwidth, 1 GiB over all ranks; the shapes themselves are in ra_kernels.cuh):
-//  - reduce-scatter: loads of 2 ranks at a time up to N = 3 (ShapeRS2) and for
-//    min/max (ShapeRS), of 4 for sum/avg/prod from N = 4 (ShapeS); fp32
-//    partials on ShapeM;
+//  - reduce-scatter: loads of 2 ranks at a time up to N = 3, with registers for
+//    8 CTAs/SM for fp16/bf16 sum/avg/prod (ShapeRS2) and for 6 otherwise
+//    (ShapeRS6: fp32 N = 3 avg 101% against 90%, bf16 max 100-101% against
+//    98-99%; bf16 avg 88% against 97-98%), and for min/max from N = 4
+//    (ShapeRS); of 4 for sum/avg/prod from N = 4 (ShapeS); fp32 partials on
+//    ShapeM;
 //  - all-reduce N <= 2: ShapeS4 (99%), except fp16/bf16 sum/avg/prod and fp32
 //    partials, which keep ShapeS (98.5-99%); min/max fp32 partials, which do
 //    not fit ShapeS's 64 registers, take ShapeM3 (92% against 80%);
@@ -67,7 +70,7 @@ int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool 
               bool minmax = false) {
   if (reduce_scatter) {
     if (acc32) return ra::SHAPE_M;
-    if (nranks <= 3) return ra::SHAPE_RS2;
+    if (nranks <= 3) return (narrow && !minmax) ? ra::SHAPE_RS2 : ra::SHAPE_RS6;
     return minmax ? ra::SHAPE_RS : ra::SHAPE_S;
   }
   if (nranks <= 2) {

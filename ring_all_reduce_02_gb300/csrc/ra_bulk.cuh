@@ -80,6 +80,7 @@ __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(
 
 template <int DT, int OP>
 __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_constant__ BulkArgs ba) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
@@ -190,8 +191,7 @@ cudaError_t launch_bulk_op(const BulkArgs& b, dim3 grid, size_t smem, cudaStream
   cudaError_t err =
       cudaFuncSetAttribute(ar_bulk_kernel<DT, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  ar_bulk_kernel<DT, OP><<<grid, kBulkThreads, smem, s>>>(b);
-  return cudaGetLastError();
+  return launch_programmatic(ar_bulk_kernel<DT, OP>, grid, kBulkThreads, smem, s, b);
 }
 
 }  // namespace ra

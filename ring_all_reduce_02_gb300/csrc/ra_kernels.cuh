@@ -42,14 +42,64 @@ namespace ra {
 // N = 4..7: 95-99% with 256 x 1 at 2 CTAs/SM (the wide shape: 90-92% at
 // N = 6, 7); N >= 8: 256 x 2 at 1 CTA/SM (99.5% at N = 8, 97% at N = 12 and
 // 16). Reduce-scatter reads N values per element and writes one. Up to N = 3
-// loads of 2 ranks at a time suit it (128 x 1 at 8 CTAs/SM: 97-98%, max at
-// N = 3 98% against 89% with 4); from N = 4 sum/avg keep batches of 4 (96-102%)
-// and min/max take 128 x 2 with batches of 2 (96-103%, against 91-99%).
+// loads of 2 ranks at a time suit it (max at N = 3 98% against 89% with 4):
+// 128 x 1 with registers for 6 CTAs/SM (98-101%), except fp16/bf16
+// sum/avg/prod at 8 CTAs/SM (97-98%, against 88% at 6); from N = 4 sum/avg
+// keep batches of 4 (96-102%) and min/max take 128 x 2 with batches of 2
+// (96-103%, against 91-99%).
 // 0: the CTAs of a chunk interleave (grid-stride); 1: each CTA streams one
 // contiguous slab of the chunk.
 #ifndef RA_SCHEDULE
 #define RA_SCHEDULE 0
 #endif
+
+// Programmatic dependent launch. With RA_PDL set (the default), the
+// collective kernels are launched with programmatic stream serialization, so
+// the driver prepares a launch while the kernel before it on the stream is
+// still running and starts it as that kernel's last CTA exits, instead of
+// after the usual gap between kernels. Each kernel's threads wait
+// (griddepcontrol.wait) until the previous grid has completed and its writes
+// are visible before any global load or store, so the stream order is kept.
+// On GB300, 16-32 MiB all-reduces launched back to back gained 2-4 points of
+// the copy bandwidth, and the 33 DDP buckets of a GPT-2-medium gradient ran
+// 1.6% faster. The kernels do not signal their dependents early
+// (griddepcontrol.launch_dependents): CTAs of the next launch then sat on the
+// SMs beside a running kernel that left registers free, and the fp32
+// reduce-scatter at N = 3 ran at half speed.
+#ifndef RA_PDL
+#define RA_PDL 1
+#endif
+
+__device__ __forceinline__ void pdl_enter() {
+#if RA_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
+// Launch `kernel` on `s`, as a programmatic dependent launch when RA_PDL is
+// set; returns the launch error (and consumes it).
+template <typename... P, typename... A>
+cudaError_t launch_programmatic(void (*kernel)(P...), dim3 grid, unsigned threads, size_t smem, cudaStream_t s,
+                                A&&... args) {
+#if RA_PDL
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+  const cudaError_t last = cudaGetLastError();
+  return err != cudaSuccess ? err : last;
+#else
+  kernel<<<grid, threads, smem, s>>>(static_cast<A&&>(args)...);
+  return cudaGetLastError();
+#endif
+}
 
 template <int THREADS, int MIN_BLOCKS, int UNROLL, int BATCH>
 struct Shape {
@@ -62,7 +112,8 @@ struct Shape {
 using ShapeS = Shape<128, 8, 1, 4>;   // sum/avg/prod reduce-scatter nranks >= 4; fp16/bf16 sum/avg/prod
                                       // all-reduce and fp32 partials at nranks 1..2
 using ShapeS4 = Shape<128, 4, 2, 2>;  // other all-reduces at nranks 1..2
-using ShapeRS2 = Shape<128, 8, 1, 2>; // reduce-scatter nranks 1..3
+using ShapeRS2 = Shape<128, 8, 1, 2>; // fp16/bf16 sum/avg/prod reduce-scatter nranks 1..3
+using ShapeRS6 = Shape<128, 6, 1, 2>; // other reduce-scatters at nranks 1..3
 using ShapeRS = Shape<128, 8, 2, 2>;  // min/max reduce-scatter nranks >= 4
 using ShapeN3 = Shape<256, 1, 4, 4>;  // all-reduce nranks 3
 using ShapeM = Shape<256, 2, 1, 4>;   // all-reduce nranks 4..7; fp32 partials where ShapeS would spill
@@ -77,6 +128,7 @@ using ShapeW = ShapeS;
 using ShapeM3 = ShapeS;
 using ShapeS4 = ShapeS;
 using ShapeRS2 = ShapeS;
+using ShapeRS6 = ShapeS;
 using ShapeRS = ShapeS;
 using ShapeMB8 = ShapeS;
 #endif
@@ -96,7 +148,8 @@ enum ShapeId {
   SHAPE_RS2 = 9,
   SHAPE_RS = 10,
   SHAPE_RS_OFFGRID_B2 = 11,
-  SHAPE_MB8 = 12
+  SHAPE_MB8 = 12,
+  SHAPE_RS6 = 13
 };
 
 enum Kind {
@@ -232,35 +285,50 @@ __device__ __forceinline__ void fold(const Args& a, int c, int n, const uint64_t
   else fold_vectors<DT, OP, kUnroll, kBatch>(a, c, n, off, ok, acc);
 }
 
-// the ring fold of one element i of chunk c
+// the ring fold of one element i of chunk c. The loads of up to kElemBatch
+// ranks are issued before any of them is folded, so an element waits about one
+// memory latency per kElemBatch ranks instead of one per rank.
+constexpr int kElemBatch = 8;
 template <int DT, int OP, bool ACC32>
 __device__ __forceinline__ uint32_t fold_elem(const Args& a, int c, int n, uint64_t i) {
+  uint32_t acc = 0;
+  float accf = 0.0f;
+  for (int k0 = 0; k0 < n; k0 += kElemBatch) {
+    uint32_t x[kElemBatch];
+#pragma unroll
+    for (int kb = 0; kb < kElemBatch; ++kb) {
+      const int k = k0 + kb;
+      if (k < n) {
+        int r = c + k;
+        if (r >= n) r -= n;
+        x[kb] = ld_elem<DT>(a.src[r], i);
+      }
+    }
+#pragma unroll
+    for (int kb = 0; kb < kElemBatch; ++kb) {
+      const int k = k0 + kb;
+      if (k < n) {
+        if constexpr (ACC32) accf = k == 0 ? widen16<DT>(x[kb]) : f32_hop<OP>(accf, widen16<DT>(x[kb]));
+        else acc = k == 0 ? x[kb] : elem_hop<DT, OP>(acc, x[kb]);
+      }
+    }
+  }
   if constexpr (ACC32) {
-    float acc = widen16<DT>(ld_elem<DT>(a.src[c], i));
-    for (int k = 1; k < n; ++k) {
-      int r = c + k;
-      if (r >= n) r -= n;
-      acc = f32_hop<OP>(acc, widen16<DT>(ld_elem<DT>(a.src[r], i)));
-    }
-    if constexpr (OP == OP_AVG) acc = __fmul_rn(acc, a.inv_n);
-    return round16<DT>(acc);
+    if constexpr (OP == OP_AVG) accf = __fmul_rn(accf, a.inv_n);
+    return round16<DT>(accf);
   } else {
-    uint32_t acc = ld_elem<DT>(a.src[c], i);
-    for (int k = 1; k < n; ++k) {
-      int r = c + k;
-      if (r >= n) r -= n;
-      acc = elem_hop<DT, OP>(acc, ld_elem<DT>(a.src[r], i));
-    }
     if constexpr (OP == OP_AVG) acc = elem_avg<DT>(acc, a.inv_n, n);
     return acc;
   }
 }
 
-// Per-element path over [b0, vb) and [ve, b1), shared by the chunk's CTAs.
+// Per-element path over [b0, vb) and [ve, b1), shared by the chunk's CTAs
+// from the row's last CTA down: the vector loops leave those with the fewest
+// trips, so the edge elements do not lengthen the longest CTA.
 template <int kThreads, typename F>
 __device__ __forceinline__ void for_each_edge_elem(uint64_t b0, uint64_t vb, uint64_t ve, uint64_t b1, F&& f) {
   const uint64_t n_lo = vb - b0, total = n_lo + (b1 - ve);
-  for (uint64_t k = (uint64_t)blockIdx.x * kThreads + threadIdx.x; k < total;
+  for (uint64_t k = (uint64_t)(gridDim.x - 1 - blockIdx.x) * kThreads + threadIdx.x; k < total;
        k += (uint64_t)gridDim.x * kThreads) {
     f(k < n_lo ? b0 + k : ve + (k - n_lo));
   }
@@ -271,6 +339,7 @@ __device__ __forceinline__ void for_each_edge_elem(uint64_t b0, uint64_t vb, uin
 // ---------------------------------------------------------------------------
 template <int DT, int OP, bool ACC32, class SH>
 __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(const __grid_constant__ Args a) {
+  pdl_enter();
   constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
@@ -308,6 +377,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(
 // ---------------------------------------------------------------------------
 template <int DT, int OP, bool ACC32, class SH, bool OFFGRID = false>
 __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(const __grid_constant__ Args a) {
+  pdl_enter();
   constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
@@ -371,6 +441,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
 // ---------------------------------------------------------------------------
 template <int DT, class SH>
 __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ag_copy_kernel(const __grid_constant__ Args a) {
+  pdl_enter();
   constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
@@ -423,13 +494,11 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ag_copy_kernel(c
 // ---------------------------------------------------------------------------
 template <int DT, int OP, bool ACC32, class SH>
 cudaError_t launch_ar(const Args& a, dim3 grid, cudaStream_t s) {
-  ar_fused_kernel<DT, OP, ACC32, SH><<<grid, SH::kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_programmatic(ar_fused_kernel<DT, OP, ACC32, SH>, grid, SH::kThreads, 0, s, a);
 }
 template <int DT, int OP, bool ACC32, class SH, bool OFFGRID = false>
 cudaError_t launch_rs(const Args& a, dim3 grid, cudaStream_t s) {
-  rs_fused_kernel<DT, OP, ACC32, SH, OFFGRID><<<grid, SH::kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_programmatic(rs_fused_kernel<DT, OP, ACC32, SH, OFFGRID>, grid, SH::kThreads, 0, s, a);
 }
 template <int DT, int OP, bool ACC32, class SH>
 cudaError_t launch_fused_shape(int kind, const Args& a, dim3 grid, cudaStream_t s) {
@@ -454,8 +523,13 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
       }
       break;
     case SHAPE_RS2:
-      if constexpr (!ACC32) {
+      if constexpr (!ACC32 && Elem<DT>::kSize == 2 && OP != OP_MIN && OP != OP_MAX) {
         if (rs) return launch_rs<DT, OP, false, ShapeRS2>(a, grid, s);
+      }
+      break;
+    case SHAPE_RS6:
+      if constexpr (!ACC32 && (Elem<DT>::kSize == 4 || OP == OP_MIN || OP == OP_MAX)) {
+        if (rs) return launch_rs<DT, OP, false, ShapeRS6>(a, grid, s);
       }
       break;
     case SHAPE_RS:
@@ -521,6 +595,7 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_M3: return shape_params_of<ShapeM3>(threads, unroll, min_blocks);
     case SHAPE_S4: return shape_params_of<ShapeS4>(threads, unroll, min_blocks);
     case SHAPE_RS2: return shape_params_of<ShapeRS2>(threads, unroll, min_blocks);
+    case SHAPE_RS6: return shape_params_of<ShapeRS6>(threads, unroll, min_blocks);
     case SHAPE_RS: return shape_params_of<ShapeRS>(threads, unroll, min_blocks);
     case SHAPE_MB8: return shape_params_of<ShapeMB8>(threads, unroll, min_blocks);
     default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);

@@ -41,8 +41,7 @@ cudaError_t launch_ag_tma(const Args& a, dim3 grid, cudaStream_t s) {
         cudaFuncSetAttribute(ag_tma_store_kernel<DT, kUnroll>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }
-  ag_tma_store_kernel<DT, kUnroll><<<grid, kAgThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_programmatic(ag_tma_store_kernel<DT, kUnroll>, grid, kAgThreads, smem, s, a);
 }
 
 template <int DT>
@@ -52,8 +51,7 @@ cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
     return launch_ag_tma<DT, 1>(a, grid, s);
   }
   if (kind == KIND_RING_AG_STEP) return launch_ring_ag_step<DT>(a, grid, s);
-  ag_copy_kernel<DT, AgShape><<<grid, AgShape::kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_programmatic(ag_copy_kernel<DT, AgShape>, grid, AgShape::kThreads, 0, s, a);
 }
 
 cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid, cudaStream_t s) {

@@ -60,6 +60,7 @@ __device__ __forceinline__ uint32_t run_prog_elem(const OrderArgs& o, int pr, in
 // IS_RS: reduce-scatter (chunk c to dst[c], compact) instead of all-reduce.
 template <int DT, int OP, bool IS_RS>
 __global__ void __launch_bounds__(kOrdThreads, 6) ordered_kernel(const __grid_constant__ OrderArgs o) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t slots[];  // [rank][thread] vectors
   constexpr int ES = Elem<DT>::kSize;
   constexpr int V = kOrdVecBytes / ES;  // elements per staged vector
@@ -134,20 +135,18 @@ __global__ void __launch_bounds__(kOrdThreads, 6) ordered_kernel(const __grid_co
   }
 }
 
+template <int DT, int OP, bool IS_RS>
+cudaError_t launch_ordered_kind(const OrderArgs& o, dim3 grid, cudaStream_t s) {
+  const size_t smem = (size_t)o.base.nranks * kOrdThreads * kOrdVecBytes;
+  const cudaError_t err =
+      cudaFuncSetAttribute(ordered_kernel<DT, OP, IS_RS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  return launch_programmatic(ordered_kernel<DT, OP, IS_RS>, grid, kOrdThreads, smem, s, o);
+}
+
 template <int DT, int OP>
 cudaError_t launch_ordered_op(bool is_rs, const OrderArgs& o, dim3 grid, cudaStream_t s) {
-  const size_t smem = (size_t)o.base.nranks * kOrdThreads * kOrdVecBytes;
-  cudaError_t err;
-  if (is_rs) {
-    err = cudaFuncSetAttribute(ordered_kernel<DT, OP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    ordered_kernel<DT, OP, true><<<grid, kOrdThreads, smem, s>>>(o);
-  } else {
-    err = cudaFuncSetAttribute(ordered_kernel<DT, OP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    ordered_kernel<DT, OP, false><<<grid, kOrdThreads, smem, s>>>(o);
-  }
-  return cudaGetLastError();
+  return is_rs ? launch_ordered_kind<DT, OP, true>(o, grid, s) : launch_ordered_kind<DT, OP, false>(o, grid, s);
 }
 
 }  // namespace ra

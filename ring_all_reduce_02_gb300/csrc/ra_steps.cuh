@@ -15,6 +15,10 @@
 // Per step the reduce-scatter reads 2 and writes 1 chunk per rank (3 S over
 // all ranks), the all-gather reads and writes 1 (2 S): 5 (N-1) S for the whole
 // schedule, against 2 N S for the fused kernel.
+//
+// The steps are plain launches, each after the previous one has completed:
+// as programmatic dependent launches whose CTAs also signalled the next step
+// early, the schedule measured 1.5% slower on GB300.
 #pragma once
 
 #include "ra_kernels.cuh"
