@@ -46,6 +46,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t run_prog_elem(const OrderArgs& o, int pr, int n, uint64_t i) {
+  // One load per rank in turn. Issuing them in batches before the stores to
+  // the slot array (as the ring's per-element fold does) changed the code
+  // generated for the vector path and cost it 8 points of the copy bandwidth.
   uint32_t v[RA_MAX_RANKS];
   for (int r = 0; r < n; ++r) v[r] = ld_elem<DT>(o.base.src[r], i);
   for (int t = 0; t < o.prog_len[pr]; ++t) {
