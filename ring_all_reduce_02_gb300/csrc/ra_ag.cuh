@@ -9,7 +9,8 @@
 // one thread hands it to the Tensor Memory Accelerator as N bulk stores
 // (cp.async.bulk shared -> global, 8 or 16 KB contiguous per destination),
 // double-buffered so the next tile loads while the last one is written. The
-// planner picks the tile and the CTAs per SM from N. ag_copy_kernel
+// planner picks the tile, the CTAs per SM and the grid from N: a row of CTAs
+// per chunk, or ag_tma_flat_kernel's single tile sequence over all SMs. ag_copy_kernel
 // (ra_kernels.cuh: every thread loads vectors into registers and stores each
 // to the N destinations) measured 84-91% at its best shape; it is kept for
 // comparison sweeps (RA_AG_TUNE_KERNEL=0).
@@ -28,7 +29,7 @@ using AgShape = Shape<kAgThreads, 2, 1, 1>;  // the register kernel
 #endif
 constexpr uint32_t kAgStages = RA_AG_STAGES;  // tiles in shared memory per CTA
 
-enum AgKernel { AG_REGISTERS = 0, AG_TMA_STORE = 1 };
+enum AgKernel { AG_REGISTERS = 0, AG_TMA_STORE = 1, AG_TMA_FLAT = 2 };
 constexpr int kShapeAgBase = 100;  // Args::shape of an all-gather launch: kShapeAgBase + AgKernel
 
 struct AgPlan {
@@ -37,12 +38,15 @@ struct AgPlan {
   int blocks_per_sm;  // resident CTAs per SM the grid is sized for
 };
 
-// Chosen from a sweep on GB300 (fp32, 1 GiB over all ranks, fraction of the
+// Chosen from sweeps on GB300 (fp32, 1 GiB over all ranks, fraction of the
 // copy bandwidth): the tiles in flight per SM that keep HBM busiest shrink as
 // N grows, because the reads are 1/(N+1) of the traffic. 32 KB per SM at
-// N <= 3 (97% at N = 2, 93% at N = 3), 16 KB at N = 4..7 (88-94%), 8 KB from
-// N = 8 (92% at N = 8, 90% at N = 12, 87% at N = 16). The register kernel
-// measured 84-91% at its best shape.
+// N <= 3 (98.6% at N = 2, 92% at N = 3), 16 KB at N = 4..7, 8 KB from N = 8.
+// Up to N = 4 and at N = 8 a row of CTAs per chunk fills the SMs (95.7% at
+// N = 4, 93.5% at N = 8). Elsewhere the rows leave SMs idle, and one tile
+// sequence over all SMs does better: 95.2 / 92.0 / 88.8% at N = 5 / 6 / 7
+// against 92.6 / 90.8 / 86.5%, 92.0 / 89.4% at N = 12 / 16 against
+// 90.2 / 88.4%. The register kernel measured 84-91% at its best shape.
 inline AgPlan ag_plan_for(int nranks) {
 #ifdef RA_AG_TUNE_KERNEL  // tuning sweeps: one plan for every rank count
   (void)nranks;
@@ -50,9 +54,10 @@ inline AgPlan ag_plan_for(int nranks) {
 #else
   if (nranks <= 2) return {AG_TMA_STORE, 1, 4};
   if (nranks == 3) return {AG_TMA_STORE, 2, 2};
-  if (nranks <= 5) return {AG_TMA_STORE, 1, 2};
-  if (nranks <= 7) return {AG_TMA_STORE, 2, 1};
-  return {AG_TMA_STORE, 1, 1};
+  if (nranks == 4) return {AG_TMA_STORE, 1, 2};
+  if (nranks <= 7) return {AG_TMA_FLAT, 2, 1};
+  if (nranks == 8) return {AG_TMA_STORE, 1, 1};
+  return {AG_TMA_FLAT, 1, 1};
 #endif
 }
 
@@ -88,14 +93,16 @@ __device__ __forceinline__ Vec ag_load(const void* in, bool in_vec, uint64_t off
   return v;
 }
 
-// The whole tiles of one chunk. G = 0: the compact chunk is on the
-// destinations' vector grid and a thread loads kUnroll vectors; G = 2..16: it
-// is off the grid and the CTA reads the tile in G-byte units, consecutive
-// threads on consecutive units. Either way the loads are issued before the
-// wait for the stage, and the stage holds the tile in destination order.
+// The CTA's whole tiles of one chunk: t0, t0 + tstride, ... below ntiles; `it`
+// counts the CTA's tiles so far and picks the stage. G = 0: the compact chunk
+// is on the destinations' vector grid and a thread loads kUnroll vectors;
+// G = 2..16: it is off the grid and the CTA reads the tile in G-byte units,
+// consecutive threads on consecutive units. Either way the loads are issued
+// before the wait for the stage, and the stage holds the tile in destination
+// order.
 template <int DT, int kUnroll, uint32_t G>
 __device__ __forceinline__ void ag_tiles(const Args& a, uint8_t* smem, const char* in, uint64_t vb, uint64_t b0,
-                                         uint64_t ntiles) {
+                                         uint64_t ntiles, uint64_t t0, uint64_t tstride, uint32_t& it) {
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   constexpr uint32_t TV = (uint32_t)kAgThreads * kUnroll;  // vectors per tile
@@ -103,8 +110,7 @@ __device__ __forceinline__ void ag_tiles(const Args& a, uint8_t* smem, const cha
   using T = typename UnitT<G == 0 ? 16 : G>::T;
   constexpr uint32_t K = G == 0 ? kUnroll : TB / (G * kAgThreads);  // loads per thread per tile
   const int n = a.nranks;
-  uint32_t it = 0;
-  for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+  for (uint64_t t = t0; t < ntiles; t += tstride, ++it) {
     const char* src = in + (vb + t * TV * V - b0) * ES;  // the tile in the compact chunk
     Vec v[G == 0 ? kUnroll : 1];
     T w[G == 0 ? 1 : K];
@@ -138,6 +144,77 @@ __device__ __forceinline__ void ag_tiles(const Args& a, uint8_t* smem, const cha
   }
 }
 
+template <int DT, int kUnroll>
+__device__ __forceinline__ void ag_chunk_tiles(const Args& a, uint8_t* smem, const char* in, bool in_vec, uint64_t vb,
+                                               uint64_t b0, uint64_t ntiles, uint64_t t0, uint64_t tstride,
+                                               uint32_t& it) {
+  constexpr int ES = Elem<DT>::kSize;
+  if (t0 >= ntiles) return;
+  if (in_vec) {
+    ag_tiles<DT, kUnroll, 0>(a, smem, in, vb, b0, ntiles, t0, tstride, it);
+  } else {
+    switch (unit_bytes(in + (vb - b0) * ES)) {
+      case 16: ag_tiles<DT, kUnroll, 16>(a, smem, in, vb, b0, ntiles, t0, tstride, it); break;
+      case 8: ag_tiles<DT, kUnroll, 8>(a, smem, in, vb, b0, ntiles, t0, tstride, it); break;
+      case 4: ag_tiles<DT, kUnroll, 4>(a, smem, in, vb, b0, ntiles, t0, tstride, it); break;
+      default: ag_tiles<DT, kUnroll, 2>(a, smem, in, vb, b0, ntiles, t0, tstride, it); break;
+    }
+  }
+}
+
+// Whole tiles per chunk can differ by one between chunks; this bound holds
+// for every chunk (a chunk has at most count / n + 1 elements).
+template <int kUnroll>
+__host__ __device__ inline uint64_t ag_tiles_per_chunk_bound(uint64_t count, int n, int v) {
+  return (count / (uint64_t)n + 1) / (uint64_t)v / ((uint64_t)kAgThreads * kUnroll) + 1;
+}
+
+// grid (CTAs, 1), the same threads and shared memory as below. The tiles of
+// all chunks form one sequence (tile k of chunk c at c * tpc + k) dealt to the
+// CTAs in turn, so each CTA (one per SM on the budget) gets an equal share
+// whatever N is; with a row of CTAs per chunk, N that do not divide the SM
+// count leave SMs idle (8 of 152 at N = 12 and 16). Chunk c's leftover vectors
+// and edge elements go to CTA c mod gridDim.x.
+template <int DT, int kUnroll>
+__global__ void __launch_bounds__(kAgThreads) ag_tma_flat_kernel(const __grid_constant__ Args a) {
+  pdl_enter();
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int V = Elem<DT>::kPerVec;
+  constexpr int ES = Elem<DT>::kSize;
+  constexpr uint32_t TV = (uint32_t)kAgThreads * kUnroll;  // vectors per tile
+  const int n = a.nranks;
+  const uint64_t tpc = ag_tiles_per_chunk_bound<kUnroll>(a.count, n, V);
+  const uint64_t g = gridDim.x;
+  uint32_t it = 0;
+  for (int c = 0; c < n; ++c) {
+    const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
+    uint64_t vb = b0, ve = b0;
+    if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
+    const uint64_t nv = (ve - vb) / V;
+    const uint64_t ntiles = nv / TV;
+    const char* in = static_cast<const char*>(a.src[c]);
+    const bool in_vec = (a.compact_aligned >> c) & 1u;
+    // this CTA's first tile of the chunk: the sequence index c * tpc + t0 is blockIdx.x mod g
+    const uint64_t t0 = ((uint64_t)blockIdx.x + g - ((uint64_t)c * tpc) % g) % g;
+    ag_chunk_tiles<DT, kUnroll>(a, smem, in, in_vec, vb, b0, ntiles, t0, g, it);
+    if ((uint64_t)c % g == blockIdx.x) {
+      for (uint64_t j = ntiles * TV + threadIdx.x; j < nv; j += kAgThreads) {
+        const uint64_t off = (vb + j * V) * ES;
+        const Vec x = ag_load<DT>(in, in_vec, off, b0);
+        for (int r = 0; r < n; ++r) st_vec(static_cast<char*>(a.dst[r]) + off, x);
+      }
+      const uint64_t n_lo = vb - b0, total = n_lo + (b1 - ve);
+      for (uint64_t k = threadIdx.x; k < total; k += kAgThreads) {
+        const uint64_t i = k < n_lo ? b0 + k : ve + (k - n_lo);
+        const uint32_t x = ld_elem<DT>(in, i - b0);
+        for (int r = 0; r < n; ++r) st_elem<DT>(a.dst[r], i, x);
+      }
+    }
+  }
+  // shared memory must outlive the bulk stores that read it
+  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // grid (CTAs per chunk, N), kAgThreads threads, kAgStages * ag_tile_bytes<kUnroll>()
 // of dynamic shared memory. The chunk's whole tiles go through shared memory and
 // bulk stores; the leftover vectors and the edge elements take plain stores.
@@ -157,18 +234,8 @@ __global__ void __launch_bounds__(kAgThreads) ag_tma_store_kernel(const __grid_c
   const char* in = static_cast<const char*>(a.src[c]);
   const bool in_vec = (a.compact_aligned >> c) & 1u;
 
-  if (ntiles > 0) {
-    if (in_vec) {
-      ag_tiles<DT, kUnroll, 0>(a, smem, in, vb, b0, ntiles);
-    } else {
-      switch (unit_bytes(in + (vb - b0) * ES)) {
-        case 16: ag_tiles<DT, kUnroll, 16>(a, smem, in, vb, b0, ntiles); break;
-        case 8: ag_tiles<DT, kUnroll, 8>(a, smem, in, vb, b0, ntiles); break;
-        case 4: ag_tiles<DT, kUnroll, 4>(a, smem, in, vb, b0, ntiles); break;
-        default: ag_tiles<DT, kUnroll, 2>(a, smem, in, vb, b0, ntiles); break;
-      }
-    }
-  }
+  uint32_t it = 0;
+  ag_chunk_tiles<DT, kUnroll>(a, smem, in, in_vec, vb, b0, ntiles, blockIdx.x, gridDim.x, it);
 
   for (uint64_t j = ntiles * TV + (uint64_t)blockIdx.x * kAgThreads + threadIdx.x; j < nv;
        j += (uint64_t)gridDim.x * kAgThreads) {

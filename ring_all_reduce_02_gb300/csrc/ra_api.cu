@@ -210,7 +210,7 @@ ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3*
   if (shape >= ra::kShapeAgBase) {
     const ra::AgPlan p = ra::ag_plan_for(a.nranks);
     threads = ra::kAgThreads, min_blocks = p.blocks_per_sm;
-    per_thread = p.kernel == ra::AG_TMA_STORE ? p.unroll : ra::AgShape::kUnroll;
+    per_thread = p.kernel != ra::AG_REGISTERS ? p.unroll : ra::AgShape::kUnroll;
   } else if (shape == ra::SHAPE_STEP) {
     threads = ra::StepShape::kThreads, per_thread = ra::StepShape::kUnroll, min_blocks = ra::StepShape::kMinBlocks;
   } else {
@@ -220,6 +220,15 @@ ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3*
   if (st != RA_SUCCESS) return st;
   const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
   const uint64_t n = (uint64_t)a.nranks;
+  if (shape == ra::kShapeAgBase + ra::AG_TMA_FLAT) {  // one row of CTAs shared by all chunks
+    const uint64_t tiles = n * (per_thread == 2 ? ra::ag_tiles_per_chunk_bound<2>(a.count, a.nranks, (int)v)
+                                                : ra::ag_tiles_per_chunk_bound<1>(a.count, a.nranks, (int)v));
+    uint64_t gx = (uint64_t)sms * min_blocks;
+    if (gx > tiles) gx = tiles;
+    if (gx < 1) gx = 1;
+    *grid = dim3((unsigned)gx, 1);
+    return RA_SUCCESS;
+  }
   const uint64_t per_chunk = (a.count + n - 1) / n;
   const uint64_t work = a.vec_ok ? (per_chunk / v + 1) : per_chunk;  // vectors, or elements
   const uint64_t per_cta = a.vec_ok ? (uint64_t)threads * per_thread : (uint64_t)threads;

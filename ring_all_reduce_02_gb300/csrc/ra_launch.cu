@@ -44,11 +44,26 @@ cudaError_t launch_ag_tma(const Args& a, dim3 grid, cudaStream_t s) {
   return launch_programmatic(ag_tma_store_kernel<DT, kUnroll>, grid, kAgThreads, smem, s, a);
 }
 
+template <int DT, int kUnroll>
+cudaError_t launch_ag_flat(const Args& a, dim3 grid, cudaStream_t s) {
+  constexpr uint32_t smem = kAgStages * ag_tile_bytes<kUnroll>();
+  if constexpr (smem > 48 * 1024) {
+    const cudaError_t err =
+        cudaFuncSetAttribute(ag_tma_flat_kernel<DT, kUnroll>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  return launch_programmatic(ag_tma_flat_kernel<DT, kUnroll>, grid, kAgThreads, smem, s, a);
+}
+
 template <int DT>
 cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
   if (kind == KIND_ALLGATHER && a.shape == kShapeAgBase + AG_TMA_STORE) {
     if (ag_plan_for(a.nranks).unroll == 2) return launch_ag_tma<DT, 2>(a, grid, s);
     return launch_ag_tma<DT, 1>(a, grid, s);
+  }
+  if (kind == KIND_ALLGATHER && a.shape == kShapeAgBase + AG_TMA_FLAT) {
+    if (ag_plan_for(a.nranks).unroll == 2) return launch_ag_flat<DT, 2>(a, grid, s);
+    return launch_ag_flat<DT, 1>(a, grid, s);
   }
   if (kind == KIND_RING_AG_STEP) return launch_ring_ag_step<DT>(a, grid, s);
   return launch_programmatic(ag_copy_kernel<DT, AgShape>, grid, AgShape::kThreads, 0, s, a);
