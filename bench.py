@@ -478,7 +478,7 @@ def run_sweep(args):
 CALLS = {  # name: (kernel, algorithmic bytes per launch as a multiple of S, the bytes per rank)
     "allreduce": ("ar_fused_kernel", lambda n: 2 * n),
     "reduce_scatter": ("rs_fused_kernel", lambda n: n + 1),
-    "allgather": ("ag_tma_store_kernel", lambda n: n + 1),
+    "allgather": ("ag_tma_store_kernel (N <= 4, N = 8) or ag_tma_flat_kernel", lambda n: n + 1),
     "allreduce_bulk": ("ar_bulk_kernel", lambda n: 2 * n),
     "allreduce_fp32acc": ("ar_fused_kernel (fp32 partials)", lambda n: 2 * n),
     "allreduce_tree": ("ordered_kernel", lambda n: 2 * n),
