@@ -57,8 +57,7 @@ bool overlaps(const Range& a, const Range& b) {
 //    (ShapeRS); of 4 for sum/avg/prod from N = 4 (ShapeS); fp32 partials on
 //    ShapeM;
 //  - all-reduce N <= 2: ShapeS4 (99%), except fp16/bf16 sum/avg/prod and fp32
-//    partials, which keep ShapeS (98.5-99%); min/max fp32 partials, which do
-//    not fit ShapeS's 64 registers, take ShapeM3 (92% against 80%);
+//    partials (sum/avg/prod only), which keep ShapeS (98.5-99%);
 //  - N = 3: ShapeN3 for fp32/int32, ShapeM3 for fp16/bf16 and for fp32
 //    partials, which ShapeN3 cannot hold (97% against 85%);
 //  - min/max at N = 6, 7: ShapeM3 (94-96% against 81-84% on ShapeM);
@@ -74,7 +73,7 @@ int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool 
     return minmax ? ra::SHAPE_RS : ra::SHAPE_S;
   }
   if (nranks <= 2) {
-    if (acc32) return minmax ? ra::SHAPE_M3 : ra::SHAPE_S;
+    if (acc32) return ra::SHAPE_S;
     return (narrow && !minmax) ? ra::SHAPE_S : ra::SHAPE_S4;
   }
   if (nranks == 3) return (acc32 || narrow) ? ra::SHAPE_M3 : ra::SHAPE_N3;
@@ -395,7 +394,13 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
     return run_bulk(a, dtype, op, max_sms, options->status, stream);
   }
   if (order != RA_ORDER_RING) return run_ordered(kind, a, dtype, op, order, max_sms, stream);
-  a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16)) ? 1 : 0;
+  // fp32 partials for fp16/bf16 sum, avg and prod. min and max are exact in
+  // any precision: partials would give the same bits (any NaN for any NaN),
+  // so those calls take the buffer-dtype kernels.
+  a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16) && op != RA_MIN &&
+             op != RA_MAX)
+                ? 1
+                : 0;
   a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ra::ag_plan_for(nranks).kernel
                                        : shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
                                                    dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,

@@ -574,8 +574,13 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
 // The fused all-reduce / reduce-scatter of one (dtype, op) pair.
 template <int DT, int OP>
 cudaError_t launch_op(int kind, const Args& a, dim3 grid, cudaStream_t s) {
-  constexpr bool kNarrow = DT == DT_F16 || DT == DT_BF16;
-  if (kNarrow && a.acc32) return launch_fused<DT, OP, kNarrow>(kind, a, grid, s);
+  // fp32 partials exist for fp16/bf16 sum, avg and prod; min and max are exact
+  // in the buffer dtype, and the planner never asks for partials there
+  constexpr bool kPartials = (DT == DT_F16 || DT == DT_BF16) && OP != OP_MIN && OP != OP_MAX;
+  if constexpr (kPartials) {
+    if (a.acc32) return launch_fused<DT, OP, true>(kind, a, grid, s);
+  }
+  if (a.acc32) return cudaErrorInvalidValue;
   return launch_fused<DT, OP, false>(kind, a, grid, s);
 }
 
