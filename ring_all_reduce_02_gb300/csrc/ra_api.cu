@@ -60,7 +60,11 @@ bool overlaps(const Range& a, const Range& b) {
 //    partials (sum/avg/prod only), which keep ShapeS (98.5-99%);
 //  - N = 3: ShapeN3 for fp32/int32, ShapeM3 for fp16/bf16 and for fp32
 //    partials, which ShapeN3 cannot hold (97% against 85%);
-//  - min/max at N = 6, 7: ShapeM3 (94-96% against 81-84% on ShapeM);
+//  - fp16/bf16 min/max (one paired min/max per word, less ALU work than fp32):
+//    ShapeW8 at N = 6, 7 (98.7 / 96.9% against 95.0 / 96.2% on ShapeM3), ShapeW at
+//    N = 8..11 (100.0 / 96.5% at N = 8 / 9 against 95.3 / 91.9% on ShapeM),
+//    ShapeM3 at N = 12..15 (96.9% against 93.8%), ShapeW from N = 16 (98.9%);
+//  - fp32/int32 min/max at N = 6, 7: ShapeM3 (94-96% against 81-84% on ShapeM);
 //  - fp16/bf16 sum/avg/prod at N = 6: all six ranks' loads at once (ShapeMB8,
 //    95-96% against 92-93%);
 //  - otherwise ShapeM up to N = 7 and, for fp16/bf16 (more ALU work per byte),
@@ -77,6 +81,12 @@ int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool 
     return (narrow && !minmax) ? ra::SHAPE_S : ra::SHAPE_S4;
   }
   if (nranks == 3) return (acc32 || narrow) ? ra::SHAPE_M3 : ra::SHAPE_N3;
+  if (narrow && minmax && nranks >= 6) {
+    if (nranks <= 7) return ra::SHAPE_W8;
+    if (nranks <= 11) return ra::SHAPE_W;
+    if (nranks <= 15) return ra::SHAPE_M3;
+    return ra::SHAPE_W;
+  }
   if (minmax && nranks >= 6 && nranks <= 7) return ra::SHAPE_M3;
   if (narrow && !acc32 && nranks == 6) return ra::SHAPE_MB8;
   if (nranks <= 7 || (narrow && nranks < 16)) return ra::SHAPE_M;
@@ -401,7 +411,12 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
              op != RA_MAX)
                 ? 1
                 : 0;
-  a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ra::ag_plan_for(nranks).kernel
+  // the flat all-gather deals whole tiles to the SMs and gives each chunk's
+  // per-element work to one CTA: with mixed address phases (every element on
+  // the per-element path) the rows of CTAs per chunk spread it instead
+  int ag_kernel = ra::ag_plan_for(nranks).kernel;
+  if (ag_kernel == ra::AG_TMA_FLAT && !a.vec_ok) ag_kernel = ra::AG_TMA_STORE;
+  a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ag_kernel
                                        : shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
                                                    dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
                                                    op == RA_MIN || op == RA_MAX);

@@ -120,6 +120,7 @@ using ShapeM = Shape<256, 2, 1, 4>;   // all-reduce nranks 4..7; fp32 partials w
 using ShapeW = Shape<256, 1, 2, 4>;   // all-reduce nranks >= 8
 using ShapeM3 = Shape<256, 3, 1, 4>;  // min/max at nranks 6..7, fp32 partials at nranks 3 (and min/max <= 2)
 using ShapeMB8 = Shape<256, 2, 1, 8>; // fp16/bf16 sum/avg/prod at nranks 6: all six ranks' loads at once
+using ShapeW8 = Shape<256, 1, 2, 8>;  // fp16/bf16 min/max at nranks 6..7
 #else  // tuning sweeps: one shape (RA_TUNE_T, _MB, _U, _B) for every rank count
 using ShapeS = Shape<RA_TUNE_T, RA_TUNE_MB, RA_TUNE_U, RA_TUNE_B>;
 using ShapeN3 = ShapeS;
@@ -131,6 +132,7 @@ using ShapeRS2 = ShapeS;
 using ShapeRS6 = ShapeS;
 using ShapeRS = ShapeS;
 using ShapeMB8 = ShapeS;
+using ShapeW8 = ShapeS;
 #endif
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
 // vector grid at a 2-byte offset, on ShapeS, ShapeRS2 (where the plain call
@@ -149,7 +151,8 @@ enum ShapeId {
   SHAPE_RS = 10,
   SHAPE_RS_OFFGRID_B2 = 11,
   SHAPE_MB8 = 12,
-  SHAPE_RS6 = 13
+  SHAPE_RS6 = 13,
+  SHAPE_W8 = 14
 };
 
 enum Kind {
@@ -567,6 +570,11 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (!rs) return launch_ar<DT, OP, false, ShapeMB8>(a, grid, s);
       }
       break;
+    case SHAPE_W8:
+      if constexpr (!ACC32 && (DT == DT_F16 || DT == DT_BF16) && (OP == OP_MIN || OP == OP_MAX)) {
+        if (!rs) return launch_ar<DT, OP, false, ShapeW8>(a, grid, s);
+      }
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -603,6 +611,7 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_RS6: return shape_params_of<ShapeRS6>(threads, unroll, min_blocks);
     case SHAPE_RS: return shape_params_of<ShapeRS>(threads, unroll, min_blocks);
     case SHAPE_MB8: return shape_params_of<ShapeMB8>(threads, unroll, min_blocks);
+    case SHAPE_W8: return shape_params_of<ShapeW8>(threads, unroll, min_blocks);
     default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
   }
 }

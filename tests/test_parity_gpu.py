@@ -268,6 +268,28 @@ def test_inplace_equals_out_of_place(ra, dtype):
         assert g1[r].tobytes() == g2[r].tobytes() == a[0].tobytes()
 
 
+@pytest.mark.parametrize("n", [3, 5, 12])
+def test_allgather_mixed_phases(ra, n):
+    # destinations at different element offsets share no vector grid, so every element takes the
+    # per-element path; at N = 5 and 12 the planner then keeps the row-per-chunk kernel instead
+    # of the flat tile sequence
+    dtype, length = "f32", 20_011
+    xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=13)
+    shards, _ = oracle.reduce_scatter(xs, "sum", dtype)
+    want, _, _ = oracle.allreduce(xs, "sum", dtype)
+    ins = []
+    for c, (b, e) in enumerate(oracle.chunk_range(length, n, c) for c in range(n)):
+        p = Padded(e - b, dtype, c % 2)
+        p.fill(shards[c])
+        ins.append(p)
+    recvs = [Padded(length, dtype, r % 3) for r in range(n)]
+    ra.ra_allgather([p.view for p in ins], [r.view for r in recvs])
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert recvs[r].canaries_intact()
+        assert_same_bits(to_host(recvs[r].view, dtype), want[r], dtype, f"rank {r}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_offset_views(ra, dtype):
     # every buffer at the same element offset (vector path with a head), then at different
