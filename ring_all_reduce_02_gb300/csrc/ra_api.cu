@@ -64,9 +64,11 @@ bool overlaps(const Range& a, const Range& b) {
 //    ShapeW8 at N = 6, 7 (98.7 / 96.9% against 95.0 / 96.2% on ShapeM3), ShapeW at
 //    N = 8..11 (100.0 / 96.5% at N = 8 / 9 against 95.3 / 91.9% on ShapeM),
 //    ShapeM3 at N = 12..15 (96.9% against 93.8%), ShapeW from N = 16 (98.9%);
-//  - fp32/int32 min/max at N = 6, 7: ShapeM3 (94-96% against 81-84% on ShapeM);
-//  - fp16/bf16 sum/avg/prod at N = 6: all six ranks' loads at once (ShapeMB8,
-//    95-96% against 92-93%);
+//  - every other call at N = 6, 7 loads all ranks at once on the wide shape
+//    (ShapeW8: fp32 99% / 97% against 95% / 96.5% on ShapeM and ShapeM3; bf16
+//    sum/avg at N = 7 96% against 95%), except fp16/bf16 sum/avg/prod at N = 6,
+//    which do better at 2 CTAs/SM (ShapeMB8, 97-98% against 95% on ShapeW8) and
+//    fp32 partials (ShapeM);
 //  - otherwise ShapeM up to N = 7 and, for fp16/bf16 (more ALU work per byte),
 //    up to N = 15 (98.9% at N = 8 against 93.4%); ShapeW from N = 8.
 int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
@@ -87,8 +89,7 @@ int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool 
     if (nranks <= 15) return ra::SHAPE_M3;
     return ra::SHAPE_W;
   }
-  if (minmax && nranks >= 6 && nranks <= 7) return ra::SHAPE_M3;
-  if (narrow && !acc32 && nranks == 6) return ra::SHAPE_MB8;
+  if (!acc32 && (nranks == 6 || nranks == 7)) return (narrow && nranks == 6) ? ra::SHAPE_MB8 : ra::SHAPE_W8;
   if (nranks <= 7 || (narrow && nranks < 16)) return ra::SHAPE_M;
   return ra::SHAPE_W;
 }

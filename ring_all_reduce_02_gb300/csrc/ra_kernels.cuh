@@ -116,11 +116,11 @@ using ShapeRS2 = Shape<128, 8, 1, 2>; // fp16/bf16 sum/avg/prod reduce-scatter n
 using ShapeRS6 = Shape<128, 6, 1, 2>; // other reduce-scatters at nranks 1..3
 using ShapeRS = Shape<128, 8, 2, 2>;  // min/max reduce-scatter nranks >= 4
 using ShapeN3 = Shape<256, 1, 4, 4>;  // all-reduce nranks 3
-using ShapeM = Shape<256, 2, 1, 4>;   // all-reduce nranks 4..7; fp32 partials where ShapeS would spill
+using ShapeM = Shape<256, 2, 1, 4>;   // all-reduce nranks 4..5, fp16/bf16 sum/avg/prod at 8..15; fp32 partials
 using ShapeW = Shape<256, 1, 2, 4>;   // all-reduce nranks >= 8
-using ShapeM3 = Shape<256, 3, 1, 4>;  // min/max at nranks 6..7, fp32 partials at nranks 3 (and min/max <= 2)
+using ShapeM3 = Shape<256, 3, 1, 4>;  // fp16/bf16 at nranks 3 and min/max at 12..15; fp32 partials at 3
 using ShapeMB8 = Shape<256, 2, 1, 8>; // fp16/bf16 sum/avg/prod at nranks 6: all six ranks' loads at once
-using ShapeW8 = Shape<256, 1, 2, 8>;  // fp16/bf16 min/max at nranks 6..7
+using ShapeW8 = Shape<256, 1, 2, 8>;  // all-reduce nranks 6..7 (but fp16/bf16 sum/avg/prod at 6)
 #else  // tuning sweeps: one shape (RA_TUNE_T, _MB, _U, _B) for every rank count
 using ShapeS = Shape<RA_TUNE_T, RA_TUNE_MB, RA_TUNE_U, RA_TUNE_B>;
 using ShapeN3 = ShapeS;
@@ -571,7 +571,7 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
       }
       break;
     case SHAPE_W8:
-      if constexpr (!ACC32 && (DT == DT_F16 || DT == DT_BF16) && (OP == OP_MIN || OP == OP_MAX)) {
+      if constexpr (!ACC32) {
         if (!rs) return launch_ar<DT, OP, false, ShapeW8>(a, grid, s);
       }
       break;
