@@ -67,8 +67,9 @@ bool overlaps(const Range& a, const Range& b) {
 //  - every other call at N = 6, 7 loads all ranks at once on the wide shape
 //    (ShapeW8: fp32 99% / 97% against 95% / 96.5% on ShapeM and ShapeM3; bf16
 //    sum/avg at N = 7 96% against 95%), except fp16/bf16 sum/avg/prod at N = 6,
-//    which do better at 2 CTAs/SM (ShapeMB8, 97-98% against 95% on ShapeW8) and
-//    fp32 partials (ShapeM);
+//    which do better at 2 CTAs/SM (ShapeMB8, 97-98% against 95% on ShapeW8);
+//    fp32 partials there 97-98% against 94-96% on ShapeM;
+//  - fp32 partials at N = 8: ShapeW (99% against 96.5% on ShapeM);
 //  - otherwise ShapeM up to N = 7 and, for fp16/bf16 (more ALU work per byte),
 //    up to N = 15 (98.9% at N = 8 against 93.4%); ShapeW from N = 8.
 int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
@@ -89,7 +90,8 @@ int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool 
     if (nranks <= 15) return ra::SHAPE_M3;
     return ra::SHAPE_W;
   }
-  if (!acc32 && (nranks == 6 || nranks == 7)) return (narrow && nranks == 6) ? ra::SHAPE_MB8 : ra::SHAPE_W8;
+  if (nranks == 6 || nranks == 7) return (narrow && !acc32 && nranks == 6) ? ra::SHAPE_MB8 : ra::SHAPE_W8;
+  if (acc32 && nranks == 8) return ra::SHAPE_W;
   if (nranks <= 7 || (narrow && nranks < 16)) return ra::SHAPE_M;
   return ra::SHAPE_W;
 }

@@ -120,7 +120,7 @@ using ShapeM = Shape<256, 2, 1, 4>;   // all-reduce nranks 4..5, fp16/bf16 sum/a
 using ShapeW = Shape<256, 1, 2, 4>;   // all-reduce nranks >= 8
 using ShapeM3 = Shape<256, 3, 1, 4>;  // fp16/bf16 at nranks 3 and min/max at 12..15; fp32 partials at 3
 using ShapeMB8 = Shape<256, 2, 1, 8>; // fp16/bf16 sum/avg/prod at nranks 6: all six ranks' loads at once
-using ShapeW8 = Shape<256, 1, 2, 8>;  // all-reduce nranks 6..7 (but fp16/bf16 sum/avg/prod at 6)
+using ShapeW8 = Shape<256, 1, 2, 8>;  // all-reduce nranks 6..7 (not fp16/bf16 sum/avg/prod at 6)
 #else  // tuning sweeps: one shape (RA_TUNE_T, _MB, _U, _B) for every rank count
 using ShapeS = Shape<RA_TUNE_T, RA_TUNE_MB, RA_TUNE_U, RA_TUNE_B>;
 using ShapeN3 = ShapeS;
@@ -571,9 +571,7 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
       }
       break;
     case SHAPE_W8:
-      if constexpr (!ACC32) {
-        if (!rs) return launch_ar<DT, OP, false, ShapeW8>(a, grid, s);
-      }
+      if (!rs) return launch_ar<DT, OP, ACC32, ShapeW8>(a, grid, s);
       break;
   }
   return cudaErrorInvalidValue;

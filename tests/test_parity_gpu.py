@@ -550,7 +550,8 @@ def _run_ex(ra, xs, op, dtype, order="ring", accum="dtype"):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("op", OPS)
 def test_fp32_accumulation(ra, dtype, op):
-    for n, length in ((1, 100), (2, 1001), (3, 4097), (8, 65536 + 5), (16, 1003), (64, 64 * 33 + 1)):
+    for n, length in ((1, 100), (2, 1001), (3, 4097), (6, 6 * 4099 + 5), (7, 30_011), (8, 65536 + 5), (16, 1003),
+                      (64, 64 * 33 + 1)):
         xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=n + 17)
         want, _ = oracle.allreduce_ex(xs, op, dtype, accum="fp32")
         got, shards = _run_ex(ra, xs, op, dtype, accum="fp32")
