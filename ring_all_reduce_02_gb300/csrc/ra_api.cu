@@ -62,8 +62,9 @@ bool overlaps(const Range& a, const Range& b) {
 //    partials, which ShapeN3 cannot hold (97% against 85%);
 //  - fp16/bf16 min/max (one paired min/max per word, less ALU work than fp32):
 //    ShapeW8 at N = 6, 7 (98.7 / 96.9% against 95.0 / 96.2% on ShapeM3), ShapeW at
-//    N = 8..11 (100.0 / 96.5% at N = 8 / 9 against 95.3 / 91.9% on ShapeM),
-//    ShapeM3 at N = 12..15 (96.9% against 93.8%), ShapeW from N = 16 (98.9%);
+//    N = 8, 9 (100.0 / 96.5% against 95.3 / 91.9% on ShapeM), ShapeM3 at
+//    N = 10..15 (96.4-96.8% at 10, 11, 12, 14, 15 against 93.3-93.8% on ShapeW at
+//    10, 11; 94.3% at 13, where ShapeW gave 95.7%), ShapeW from N = 16 (98.9%);
 //  - every other call at N = 6, 7 loads all ranks at once on the wide shape
 //    (ShapeW8: fp32 99% / 97% against 95% / 96.5% on ShapeM and ShapeM3; bf16
 //    sum/avg at N = 7 96% against 95%), except fp16/bf16 sum/avg/prod at N = 6,
@@ -71,7 +72,9 @@ bool overlaps(const Range& a, const Range& b) {
 //    fp32 partials there 97-98% against 94-96% on ShapeM;
 //  - fp32 partials at N = 8: ShapeW (99% against 96.5% on ShapeM);
 //  - otherwise ShapeM up to N = 7 and, for fp16/bf16 (more ALU work per byte),
-//    up to N = 15 (98.9% at N = 8 against 93.4%); ShapeW from N = 8.
+//    up to N = 15 (98.9% at N = 8 against 93.4%); ShapeW from N = 8, but
+//    ShapeM at N = 10, 11, 14 (fp32: 96.1-97.1% against 92.5-93.8%; ShapeW is
+//    ahead at 9, 12, 13, 15 by 0.4-3 points).
 int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
               bool minmax = false) {
   if (reduce_scatter) {
@@ -86,13 +89,14 @@ int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool 
   if (nranks == 3) return (acc32 || narrow) ? ra::SHAPE_M3 : ra::SHAPE_N3;
   if (narrow && minmax && nranks >= 6) {
     if (nranks <= 7) return ra::SHAPE_W8;
-    if (nranks <= 11) return ra::SHAPE_W;
+    if (nranks <= 9) return ra::SHAPE_W;
     if (nranks <= 15) return ra::SHAPE_M3;
     return ra::SHAPE_W;
   }
   if (nranks == 6 || nranks == 7) return (narrow && !acc32 && nranks == 6) ? ra::SHAPE_MB8 : ra::SHAPE_W8;
   if (acc32 && nranks == 8) return ra::SHAPE_W;
   if (nranks <= 7 || (narrow && nranks < 16)) return ra::SHAPE_M;
+  if (nranks == 10 || nranks == 11 || nranks == 14) return ra::SHAPE_M;
   return ra::SHAPE_W;
 }
 

@@ -177,9 +177,9 @@ def test_op_dtype_sweep_uneven_chunks(ra, case):
 def test_small_and_ragged_shapes(ra, dtype, op):
     seed = 1000
     # every rank count with a launch shape of its own: 6 and 7 (the wide shape loading all ranks,
-    # fp16/bf16 sum/avg/prod at 6 on two CTAs per SM), 9 and 12 (fp16/bf16 min/max shapes, the
-    # flat all-gather)
-    for n in (1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16):
+    # fp16/bf16 sum/avg/prod at 6 on two CTAs per SM), 9, 10, 12 and 14 (fp32 and fp16/bf16
+    # min/max shapes, the flat all-gather)
+    for n in (1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 12, 14, 16):
         for length in (0, 1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 33, 64, 65, 100, 257, 1000, 4097):
             xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=seed)
             seed += 1
