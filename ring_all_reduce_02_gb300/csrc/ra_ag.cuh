@@ -144,6 +144,9 @@ __device__ __forceinline__ void ag_tiles(const Args& a, uint8_t* smem, const cha
   }
 }
 
+// The CTA's whole tiles of one chunk (t0, t0 + tstride, ...), loaded by vectors
+// when the compact chunk is on the destinations' grid, else in the widest unit
+// its address allows.
 template <int DT, int kUnroll>
 __device__ __forceinline__ void ag_chunk_tiles(const Args& a, uint8_t* smem, const char* in, bool in_vec, uint64_t vb,
                                                uint64_t b0, uint64_t ntiles, uint64_t t0, uint64_t tstride,
