@@ -249,14 +249,20 @@ int ra_last_cuda_error(void);
 /*
  * Self-test of the bulk engine's bounded waits (host-visible failure
  * reporting without a GPU fault): runs the RA_ENGINE_BULK all-reduce with the
- * first tile of CTA (0, 0) never copied in, so that CTA's consumers wait for
- * it in vain, give up after 1 s, write a nonzero code to *status (device int,
- * caller-owned, which should be 0 before the call) and wind the kernel down;
- * the launch completes and the context stays usable. The receive buffers'
- * contents are unspecified afterwards. Same arguments as ra_allreduce.
+ * first tile of CTA (0, withhold_chunk) never copied in, so that CTA's
+ * consumers wait for it in vain and give up after 1 s; the CTA records a
+ * nonzero code (1 or 2, as for ra_options_t.status), waits (bounded) for its
+ * other copies in flight and winds down. The launch completes and the context
+ * stays usable. The receive buffers' contents are unspecified afterwards.
+ * status: caller-owned device ints, 0 before the call. status_per_chunk 0:
+ * every chunk reports into status[0] (one int); 1: chunk c reports into
+ * status[c] (nranks ints), as ra_allreduce_bulk_noalloc's words do.
+ * withhold_chunk in [0, nranks); count must give that chunk at least one
+ * whole tile for the self-test to fire. Same other arguments as ra_allreduce.
  */
 ra_status_t ra_selftest_bulk_timeout(const void* const* sendbufs, void* const* recvbufs, size_t count,
-                                     ra_dtype_t dtype, ra_op_t op, int nranks, int* status, void* stream);
+                                     ra_dtype_t dtype, ra_op_t op, int nranks, int withhold_chunk, int* status,
+                                     int status_per_chunk, void* stream);
 
 /* Bytes per vector access of the library's compiled kernels (16 or 32): the address
  * phase (address mod this) the buffers must share for the vector path. */
@@ -282,11 +288,12 @@ int ra_vector_bytes(void);
  * compute that the bulk engine is meant to run beside; and a host program
  * that all-reduces pinned host buffers and owns no device memory at all.
  *
- * Set-up: the first call on a device, with that device current, looks up the
- * device address of the array (cudaGetSymbolAddress) and keeps it for later
- * calls on that device; a failed lookup returns RA_ERR_CUDA. The lookup can
- * load the library's kernels onto the device, so make the first call before
- * any stream capture begins.
+ * Set-up: every call looks up the array's device address in the current
+ * context (cudaGetSymbolAddress) and keeps nothing between calls, so a call
+ * after a context switch or a device reset uses that context's copy. A failed
+ * lookup returns RA_ERR_CUDA. The first lookup in a context can load the
+ * library's kernels into it, so make the first call there before any stream
+ * capture begins.
  *
  * Each call enqueues on `stream`: a clear of words [0, nranks) of the array;
  * the kernel, whose CTAs for chunk c record in word c the code of a bounded
@@ -302,12 +309,18 @@ int ra_vector_bytes(void);
  * engine's own limit); a larger nranks (up to RA_MAX_RANKS) returns
  * RA_ERR_SCRATCH_LIMIT before anything is enqueued.
  *
- * Concurrency: each device has one copy of the array, shared by all calls on
- * that device. Two calls in flight at once there (on different streams, or
- * from different threads) race on it: one call's clear can erase the
- * other's codes, and a copy can return the other's codes. The reduced
- * buffers are not affected. Calls on one stream run one after the other and
- * do not race.
+ * Errors: every check, the plan and the kernel's shared-memory set-up come
+ * before the first enqueue, so an error returned from them enqueues nothing.
+ * Only a failure of one of the three enqueues itself (RA_ERR_CUDA) can leave
+ * the earlier ones queued; they touch nothing but the library's words and,
+ * for the copy, chunk_status.
+ *
+ * Concurrency: each context has one copy of the array (on the usual primary
+ * context: one per device), shared by all calls there. Two calls in flight at
+ * once in one context (on different streams, or from different threads) race
+ * on it: one call's clear can erase the other's codes, and a copy can return
+ * the other's codes. The reduced buffers are not affected. Calls on one
+ * stream run one after the other and do not race.
  */
 ra_status_t ra_allreduce_bulk_noalloc(const void* const* sendbufs, void* const* recvbufs, size_t count,
                                       ra_dtype_t dtype, ra_op_t op, int nranks, int max_sms, int* chunk_status,

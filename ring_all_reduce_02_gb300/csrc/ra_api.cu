@@ -6,8 +6,6 @@
 #include <stdint.h>
 #include <string.h>
 
-#include <mutex>
-
 #include "../../include/ra.h"
 #include "ra_ag.cuh"
 #include "ra_bulk.cuh"
@@ -19,6 +17,7 @@ namespace ra {
 cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_ordered_kernel(bool is_rs, int dtype, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
 cudaError_t launch_bulk_kernel(int dtype, int op, const BulkArgs& b, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t configure_bulk_kernel(int dtype, int op, size_t smem);
 }  // namespace ra
 
 namespace {
@@ -274,13 +273,22 @@ constexpr size_t kBulkSmemBudget = (size_t)RA_BULK_SMEM_KB * 1024;
 #endif
 constexpr int kBulkMaxStages = RA_BULK_MAX_STAGES;
 
-ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* status, void* stream,
-                     int withhold_first = 0, uint32_t status_stride = 0) {
-  ra::BulkArgs b;
+// A planned bulk-engine launch: kernel arguments, grid and shared memory.
+struct BulkLaunch {
+  ra::BulkArgs args;
+  dim3 grid;
+  size_t smem = 0;
+};
+
+// Plans a bulk-engine launch and raises the kernel's shared-memory limit to
+// what it needs. Enqueues nothing: every error the bulk path can report before
+// its launch is reported here.
+ra_status_t plan_bulk(const ra::Args& a, int dtype, int op, int max_sms, BulkLaunch* p) {
+  ra::BulkArgs& b = p->args;
   b.base = a;
-  b.status = status;
-  b.status_stride = status_stride;
-  b.withhold_first = withhold_first;
+  b.status = nullptr;
+  b.status_stride = 0;
+  b.withhold_chunk = -1;
   const int n = a.nranks;
   // about 32 KB per stage: 32 KB / N per rank, between 4 and 16 KB (fewer, longer tiles when N
   // is small, so the per-tile barrier work is spread over more bytes), and at least one vector
@@ -297,7 +305,7 @@ ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* sta
   if (stages > (size_t)kBulkMaxStages) stages = kBulkMaxStages;
   if (stages < 2) return RA_ERR_UNSUPPORTED;
   b.stages = (uint32_t)stages;
-  const size_t smem = 128 * ((2 * stages * 8 + 127) / 128) + stages * stage_bytes;
+  p->smem = 128 * ((2 * stages * 8 + 127) / 128) + stages * stage_bytes;
   int sms = 0;
   const ra_status_t st = sm_budget(max_sms, &sms);
   if (st != RA_SUCCESS) return st;
@@ -306,9 +314,29 @@ ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* sta
   uint64_t gx = (uint64_t)sms / (uint64_t)n;
   if (gx > tiles) gx = tiles;
   if (gx < 1) gx = 1;
-  const cudaError_t err = ra::launch_bulk_kernel(dtype, op, b, dim3((unsigned)gx, (unsigned)n), smem,
-                                                 static_cast<cudaStream_t>(stream));
+  p->grid = dim3((unsigned)gx, (unsigned)n);
+  const cudaError_t err = ra::configure_bulk_kernel(dtype, op, p->smem);
   return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
+}
+
+// Enqueues a planned bulk-engine launch. status: the device words the CTAs of
+// chunk c report into (word c * status_stride); withhold_chunk >= 0 runs the
+// self-test that leaves that chunk's first tile uncopied.
+ra_status_t launch_bulk(BulkLaunch p, int dtype, int op, int* status, uint32_t status_stride,
+                        int withhold_chunk, void* stream) {
+  p.args.status = status;
+  p.args.status_stride = status_stride;
+  p.args.withhold_chunk = withhold_chunk;
+  const cudaError_t err =
+      ra::launch_bulk_kernel(dtype, op, p.args, p.grid, p.smem, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
+}
+
+ra_status_t run_bulk(const ra::Args& a, int dtype, int op, int max_sms, int* status, void* stream) {
+  BulkLaunch p;
+  const ra_status_t st = plan_bulk(a, dtype, op, max_sms, &p);
+  if (st != RA_SUCCESS) return st;
+  return launch_bulk(p, dtype, op, status, 0, -1, stream);
 }
 
 // ---- reduction programs of the other orders --------------------------------
@@ -638,44 +666,40 @@ int ra_last_cuda_error(void) { return g_last_cuda_error; }
 int ra_vector_bytes(void) { return ra::kVecBytes; }
 
 ra_status_t ra_selftest_bulk_timeout(const void* const* sendbufs, void* const* recvbufs, size_t count,
-                                     ra_dtype_t dtype, ra_op_t op, int nranks, int* status, void* stream) {
-  if (status == nullptr) return RA_ERR_INVALID_ARG;
+                                     ra_dtype_t dtype, ra_op_t op, int nranks, int withhold_chunk, int* status,
+                                     int status_per_chunk, void* stream) {
+  if (status == nullptr || (status_per_chunk != 0 && status_per_chunk != 1)) return RA_ERR_INVALID_ARG;
+  if (withhold_chunk < 0 || withhold_chunk >= nranks) return RA_ERR_INVALID_ARG;
   ra::Args a;
-  const ra_status_t st = prepare(ra::KIND_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, nranks, &a);
+  ra_status_t st = prepare(ra::KIND_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, nranks, &a);
   if (st != RA_SUCCESS) return st;
   if (nranks > 16 || !a.vec_ok || count == 0) return RA_ERR_UNSUPPORTED;
-  return run_bulk(a, dtype, op, 0, status, stream, /*withhold_first=*/1);
+  BulkLaunch p;
+  st = plan_bulk(a, dtype, op, 0, &p);
+  if (st != RA_SUCCESS) return st;
+  return launch_bulk(p, dtype, op, status, (uint32_t)status_per_chunk, withhold_chunk, stream);
 }
 
 }  // extern "C"
 
 // ---- the bulk all-reduce without caller scratch ------------------------------
 // The status words of ra_allreduce_bulk_noalloc: one per chunk, part of the
-// module's device image, so no call allocates them. One copy per device; calls
-// in flight at once on one device share it (see the declaration in ra.h).
+// module's device image, so no call allocates them. One copy per context that
+// has loaded the module; calls in flight at once in one context share it (see
+// the declaration in ra.h).
 namespace {
 
 static __device__ __align__(256) int g_noalloc_status[RA_NOALLOC_STATUS_WORDS];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-int* g_noalloc_ptr[kMaxDevices] = {};
-
-// The array's device address on the current device, looked up on the first
-// call there and kept.
+// The array's device address in the current context. Looked up on every call
+// rather than kept: an address from an earlier call may belong to another
+// context (the caller switched contexts, or reset the device since), and the
+// lookup is a table search once the module is loaded.
 ra_status_t noalloc_status_words(int** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_status);
   if (err != cudaSuccess) return cuda_failed(err);
-  if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_noalloc_status);
-    if (err != cudaSuccess) return cuda_failed(err);
-    g_noalloc_ptr[dev] = static_cast<int*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+  *out = static_cast<int*>(p);
   return RA_SUCCESS;
 }
 
@@ -691,6 +715,10 @@ extern "C" ra_status_t ra_allreduce_bulk_noalloc(const void* const* sendbufs, vo
   if (st != RA_SUCCESS) return st;
   if (count == 0) return RA_SUCCESS;
   if (!a.vec_ok) return RA_ERR_UNSUPPORTED;
+  // everything that can fail short of an enqueue failing happens before the first enqueue
+  BulkLaunch p;
+  st = plan_bulk(a, dtype, op, max_sms, &p);
+  if (st != RA_SUCCESS) return st;
   int* words = nullptr;
   st = noalloc_status_words(&words);
   if (st != RA_SUCCESS) return st;
@@ -698,7 +726,7 @@ extern "C" ra_status_t ra_allreduce_bulk_noalloc(const void* const* sendbufs, vo
   const size_t bytes = (size_t)nranks * sizeof(int);
   cudaError_t err = cudaMemsetAsync(words, 0, bytes, s);
   if (err != cudaSuccess) return cuda_failed(err);
-  st = run_bulk(a, dtype, op, max_sms, words, stream, /*withhold_first=*/0, /*status_stride=*/1);
+  st = launch_bulk(p, dtype, op, words, /*status_stride=*/1, /*withhold_chunk=*/-1, stream);
   if (st != RA_SUCCESS) return st;
   if (chunk_status != nullptr) {
     err = cudaMemcpyAsync(chunk_status, words, bytes, cudaMemcpyDefault, s);

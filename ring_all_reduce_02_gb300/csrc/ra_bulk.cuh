@@ -34,7 +34,8 @@ struct BulkArgs {
   uint32_t status_stride;  // 0: every chunk reports into status[0]; 1: chunk c into status[c]
   uint32_t tile_vecs;  // vectors per rank per stage (a multiple of kBulkConsumers)
   uint32_t stages;     // stages in the shared-memory ring
-  int withhold_first;  // self-test of the bounded waits: CTA (0, 0) never issues its first tile's copies
+  int withhold_chunk;  // self-test of the bounded waits: -1 none, else CTA (0, c) never issues its
+                       // first tile's copies for c = withhold_chunk
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -115,16 +116,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
     // ---- producer warp: one elected thread issues the bulk copies --------------
     if (threadIdx.x == kBulkConsumers) {
       uint32_t issued = 0;
-      bool ok = true;
       for (uint64_t t = first; t < ntiles; t += step, ++issued) {
         const uint32_t s = issued % S;
         if (issued >= S && !mbar_wait(&empty[s], ((issued / S) - 1) & 1)) {
           record_error(status, kBulkErrEmpty);
-          ok = false;
           break;
         }
         mbar_arrive_expect_tx(&full[s], tile_bytes * (uint32_t)n);
-        if (ba.withhold_first && issued == 0 && blockIdx.x == 0 && blockIdx.y == 0) continue;
+        if (issued == 0 && blockIdx.x == 0 && (int)blockIdx.y == ba.withhold_chunk) continue;
         const uint64_t off = (vb + t * TV * V) * ES;
         for (int k = 0; k < n; ++k) {
           int r = c + k;
@@ -133,15 +132,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
                     tile_bytes, &full[s]);
         }
       }
-      // never leave with bulk copies into this CTA's shared memory still in flight
+      // Never leave with bulk copies into this CTA's shared memory still in
+      // flight: wait (bounded) on every stage that may still be filling, also
+      // after one of these waits has run out, and keep the first error code.
       const uint32_t lo = issued > S ? issued - S : 0;
       for (uint32_t i = lo; i < issued; ++i) {
-        if (!mbar_wait(&full[i % S], (i / S) & 1)) {
-          record_error(status, kBulkErrFull);
-          break;
-        }
+        if (!mbar_wait(&full[i % S], (i / S) & 1)) record_error(status, kBulkErrFull);
       }
-      (void)ok;
     }
   } else {
     // ---- consumers: fold each landed tile in ring order, store to every rank ----
@@ -186,11 +183,15 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
   });
 }
 
+// Raises the kernel's dynamic shared-memory limit to `smem`; enqueues nothing.
+template <int DT, int OP>
+cudaError_t configure_bulk_op(size_t smem) {
+  return cudaFuncSetAttribute(ar_bulk_kernel<DT, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+// Launches the kernel; configure_bulk_op(smem) must have succeeded on this device.
 template <int DT, int OP>
 cudaError_t launch_bulk_op(const BulkArgs& b, dim3 grid, size_t smem, cudaStream_t s) {
-  cudaError_t err =
-      cudaFuncSetAttribute(ar_bulk_kernel<DT, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
   return launch_programmatic(ar_bulk_kernel<DT, OP>, grid, kBulkThreads, smem, s, b);
 }
 

@@ -26,4 +26,7 @@ cudaError_t RA_CAT3(launch_bulk_slice, RA_SLICE_DT, RA_SLICE_OP)(const BulkArgs&
                                                                  cudaStream_t s) {
   return launch_bulk_op<RA_SLICE_DT, RA_SLICE_OP>(b, grid, smem, s);
 }
+cudaError_t RA_CAT3(configure_bulk_slice, RA_SLICE_DT, RA_SLICE_OP)(size_t smem) {
+  return configure_bulk_op<RA_SLICE_DT, RA_SLICE_OP>(smem);
+}
 }  // namespace ra

@@ -95,7 +95,7 @@ def lib() -> ctypes.CDLL:
             L.ra_last_cuda_error.restype = I
             L.ra_vector_bytes.argtypes = []
             L.ra_vector_bytes.restype = I
-            L.ra_selftest_bulk_timeout.argtypes = [PP, PP, SZ, I, I, I, VP, VP]
+            L.ra_selftest_bulk_timeout.argtypes = [PP, PP, SZ, I, I, I, I, VP, I, VP]
             L.ra_selftest_bulk_timeout.restype = I
             L.ra_allreduce_bulk_noalloc.argtypes = [PP, PP, SZ, I, I, I, I, VP, VP]
             L.ra_allreduce_bulk_noalloc.restype = I
@@ -296,12 +296,18 @@ def ra_status_string(status: int) -> str:
     return lib().ra_status_string(status).decode()
 
 
-def ra_selftest_bulk_timeout(sendbufs, recvbufs, status, op: str = "sum", stream=None) -> None:
-    """Run the bulk engine with one tile withheld: its bounded wait must give up and set ``status``."""
+def ra_selftest_bulk_timeout(sendbufs, recvbufs, status, op: str = "sum", withhold_chunk: int = 0,
+                             per_chunk: bool = False, stream=None) -> None:
+    """Run the bulk engine with chunk ``withhold_chunk``'s first tile withheld: that chunk's bounded
+    wait must give up and set its status word. ``status``: a device int32 tensor, one word
+    (``per_chunk`` False) or nranks words, word c for chunk c (``per_chunk`` True)."""
     count = _check_full(sendbufs, recvbufs, "ra_selftest_bulk_timeout")
+    if status.numel() < (len(sendbufs) if per_chunk else 1):
+        raise ValueError("ra_selftest_bulk_timeout: status is too small")
     st = lib().ra_selftest_bulk_timeout(ptr_array([t.data_ptr() for t in sendbufs]),
                                         ptr_array([t.data_ptr() for t in recvbufs]), count, dtype_code(sendbufs[0]),
-                                        OP_CODES[op], len(sendbufs), ctypes.c_void_p(status.data_ptr()),
+                                        OP_CODES[op], len(sendbufs), withhold_chunk,
+                                        ctypes.c_void_p(status.data_ptr()), 1 if per_chunk else 0,
                                         ctypes.c_void_p(_stream_ptr(stream) or None))
     if st:
         raise RaError(st, "ra_selftest_bulk_timeout")

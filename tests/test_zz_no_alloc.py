@@ -99,3 +99,89 @@ def test_misaligned_phase_is_unsupported(ra):
     recvs = [torch.empty(length, dtype=torch.float32, device="cuda") for _ in range(n)]
     with pytest.raises(ra.RaError, match="unsupported"):
         ra.ra_allreduce_bulk_noalloc(sends, recvs, "sum")
+
+
+# A program that drives the GPU through the driver API alone, with no torch: it
+# runs the no-alloc call in the device's primary context, then in a second
+# context it created itself, then in the primary context again. The library's
+# status words have one address per context, so an address remembered from an
+# earlier call would point the second call's clear and kernel at memory that
+# context does not map; a lookup per call gives each context its own words.
+_CONTEXT_PROGRAM = r"""
+import ctypes, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+import oracle
+from ring_all_reduce_02_gb300 import inputs, ra
+
+cu = ctypes.CDLL("libcuda.so.1")
+def ck(res, what):
+    if res != 0:
+        raise SystemExit(f"{what}: CUresult {res}")
+ck(cu.cuInit(0), "cuInit")
+dev = ctypes.c_int()
+ck(cu.cuDeviceGet(ctypes.byref(dev), 0), "cuDeviceGet")
+primary, second = ctypes.c_void_p(), ctypes.c_void_p()
+ck(cu.cuDevicePrimaryCtxRetain(ctypes.byref(primary), dev), "cuDevicePrimaryCtxRetain")
+
+def one_call(tag, n, length, op, seed):
+    xs = inputs.rank_buffers(n, length, "f32", ("normal", 1.0), seed_base=seed)
+    nbytes = length * 4
+    send, recv = [], []
+    for x in xs:
+        p = ctypes.c_uint64()
+        ck(cu.cuMemAlloc_v2(ctypes.byref(p), ctypes.c_size_t(nbytes)), "cuMemAlloc")
+        ck(cu.cuMemcpyHtoD_v2(p, x.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(nbytes)), "HtoD")
+        send.append(p.value)
+    for _ in xs:
+        p = ctypes.c_uint64()
+        ck(cu.cuMemAlloc_v2(ctypes.byref(p), ctypes.c_size_t(nbytes)), "cuMemAlloc")
+        recv.append(p.value)
+    words = (ctypes.c_int * n)(*([-7] * n))
+    st = ra.lib().ra_allreduce_bulk_noalloc(ra.ptr_array(send), ra.ptr_array(recv), length, 0,
+                                            ra.OP_CODES[op], n, 0, ctypes.cast(words, ctypes.c_void_p), None)
+    if st != 0:
+        raise SystemExit(f"{tag}: status {st} ({ra.ra_status_string(st)}), cudaError {ra.lib().ra_last_cuda_error()}")
+    ck(cu.cuCtxSynchronize(), f"{tag}: synchronize")
+    want, _, _ = oracle.allreduce(xs, op, "f32")
+    for r in range(n):
+        got = np.empty(length, dtype=np.float32)
+        ck(cu.cuMemcpyDtoH_v2(got.ctypes.data_as(ctypes.c_void_p), ctypes.c_uint64(recv[r]),
+                              ctypes.c_size_t(nbytes)), "DtoH")
+        if got.tobytes() != want[r].tobytes():
+            raise SystemExit(f"{tag}: rank {r} differs from the oracle")
+    if list(words) != [0] * n:
+        raise SystemExit(f"{tag}: chunk codes {list(words)}")
+    for p in send + recv:
+        ck(cu.cuMemFree_v2(ctypes.c_uint64(p)), "cuMemFree")
+    print(tag, "ok", flush=True)
+
+ck(cu.cuCtxSetCurrent(primary), "cuCtxSetCurrent(primary)")
+one_call("primary", 4, 4 * 4096 * 3 + 5, "sum", 70)
+ck(cu.cuCtxCreate_v2(ctypes.byref(second), 0, dev), "cuCtxCreate")  # also makes it current
+one_call("second", 8, (1 << 18) + 3, "avg", 71)
+one_call("second again", 3, 3 * 4096 * 2 + 1, "max", 72)
+ck(cu.cuCtxSetCurrent(primary), "cuCtxSetCurrent(primary)")
+one_call("primary again", 5, 5 * 4096 + 9, "sum", 73)
+ck(cu.cuCtxDestroy_v2(second), "cuCtxDestroy")
+ck(cu.cuDevicePrimaryCtxRelease_v2(dev), "cuDevicePrimaryCtxRelease")
+print("CONTEXTS OK", flush=True)
+"""
+
+
+@pytest.mark.gpu
+def test_status_words_follow_the_current_context(ra):
+    # A caller that manages contexts with the driver API (its own context per
+    # library or per job, or a device reset between jobs) gets, in each context,
+    # that context's copy of the status words: results and codes as in the first.
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import os
+    import subprocess
+    import sys
+
+    oracle.build()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    proc = subprocess.run([sys.executable, "-c", _CONTEXT_PROGRAM, root], capture_output=True, text=True,
+                          timeout=300)
+    assert proc.returncode == 0 and "CONTEXTS OK" in proc.stdout, proc.stdout + proc.stderr
