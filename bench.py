@@ -166,6 +166,32 @@ def profiled_traffic(workload: str):
 # ---------------------------------------------------------------------------
 # the CPU oracle as a baseline (bounded sample of the same workload)
 # ---------------------------------------------------------------------------
+def host_cpu() -> dict:
+    """The host the CPU baseline ran on: logical CPUs (nproc) and the lscpu model name."""
+    try:
+        nproc = len(os.sched_getaffinity(0))
+    except AttributeError:
+        nproc = os.cpu_count() or 1
+    model = vendor = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            k, _, v = ln.partition(":")
+            if k.strip() == "Model name" and model is None:
+                model = v.strip()
+            elif k.strip() == "Vendor ID" and vendor is None:
+                vendor = v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    return {"nproc": nproc, "cpu_model": model or "unknown", "cpu_vendor": vendor or "unknown"}
+
+
 def oracle_rate(n, length, dtype, op, dist, target_s: float, max_len: int):
     """Time the oracle on a sample of the workload sized to about target_s; returns (GB/s, sample_len, secs)."""
     import oracle
@@ -214,7 +240,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
         "config": config_block(args.workload),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n} ranks x {sample} {dtype} elements per step (the workload is {length})"},
+                         "sample": f"{n} ranks x {sample} {dtype} elements per step (the workload is {length})",
+                         **host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -341,7 +368,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, sample, secs = oracle_rate(n, length, dtype, op, dist_spec, target_s=10.0, max_len=length)
         cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": min(n, os.cpu_count() or 1), "kind": "oracle",
-               "sample": f"{n} ranks x {sample} {dtype} elements ({secs:.1f} s, one thread per rank)"}
+               "sample": f"{n} ranks x {sample} {dtype} elements ({secs:.1f} s, one thread per rank)",
+               **host_cpu()}
 
     if rank == 0:
         line = {

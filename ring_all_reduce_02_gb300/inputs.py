@@ -20,6 +20,9 @@ parity, since both sides receive the same bits.
 
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "i32": np.int32}
@@ -68,8 +71,17 @@ def rank_buffer(rank: int, length: int, dtype: str, dist: tuple, seed_base: int 
     return out
 
 
-def rank_buffers(n: int, length: int, dtype: str, dist: tuple, seed_base: int = 0) -> list[np.ndarray]:
-    return [rank_buffer(r, length, dtype, dist, seed_base) for r in range(n)]
+def rank_buffers(n: int, length: int, dtype: str, dist: tuple, seed_base: int = 0,
+                 workers: int | None = None) -> list[np.ndarray]:
+    """All ranks' buffers. Ranks are drawn on ``workers`` threads (default: one per rank up to
+    the host's cores) once a buffer is large; each rank has its own generator, so the bits do
+    not depend on the thread count."""
+    if workers is None:
+        workers = min(n, os.cpu_count() or 1) if length >= _BLOCK else 1
+    if workers <= 1 or n <= 1:
+        return [rank_buffer(r, length, dtype, dist, seed_base) for r in range(n)]
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(lambda r: rank_buffer(r, length, dtype, dist, seed_base), range(n)))
 
 
 # ---- the named workloads ---------------------------------------------------

@@ -1,13 +1,13 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
 Bar: bit-exact for every dtype and op (the ring order and per-hop rounding are
-reproduced, so the tolerance is 0 ULP; any NaN equals any NaN). Small and
-medium shapes are compared element by element against the oracle's
-message-passing ring; the full-size workloads are compared on sampled elements
-(every chunk boundary +-4, the ends, 2^17 random positions) against the
-oracle's per-element definition, plus properties that hold at any size (all
-ranks byte-identical). Guard pages around every buffer ("canaries") stand in
-for a bounds checker.
+reproduced, so the tolerance is 0 ULP; any NaN equals any NaN). Every shape,
+the full-size workloads included, is compared element by element, on every
+rank, against the oracle's message-passing ring (or its tree, Rabenseifner
+and fp32-message variants). Only the case past 2^32 elements per rank (48 GiB
+on the device) is compared on sampled elements, against the oracle's
+per-element definition. Guard regions around every small buffer ("canaries")
+stand in for a bounds checker.
 """
 
 import itertools
@@ -376,7 +376,7 @@ def test_errors_enqueue_nothing(ra):
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads in the benchmark's launch configuration: sampled outputs
+# full-size workloads in the benchmark's launch configuration: every element against the oracle
 # ---------------------------------------------------------------------------
 def _host_ram_gb():
     with open("/proc/meminfo") as f:
@@ -454,8 +454,30 @@ def test_more_than_2_pow_32_elements(ra):
         assert torch.equal(gathered[r].view(torch.int16), recvs[0].view(torch.int16)), f"AG rank {r}"
 
 
-def check_full_size(ra, n, length, dtype, op, dist):
-    need_gb = 2.5 * n * length * ELEM_SIZE[dtype] / 2**30
+ORACLE_TIMEOUT_MS = 600_000  # a full-size ring step moves up to 1 GiB per message on the host
+
+
+def same_bits_fast(got, want, dtype, what):
+    """Byte equality first (one pass); the NaN-aware comparison only to explain a difference."""
+    if got.shape == want.shape and np.array_equal(got.view(np.uint8), want.view(np.uint8)):
+        return
+    assert_same_bits(got, want, dtype, what)
+
+
+def compare_ranks(recvs, want, dtype, what):
+    """Every element of every rank's device result against the oracle's, one rank at a time."""
+    for r, t in enumerate(recvs):
+        same_bits_fast(to_host(t, dtype), want[r], dtype, f"{what} rank {r}")
+
+
+def check_full_size(ra, n, length, dtype, op, dist, rs_ag=False):
+    """The workload in the bench's launch configuration, all N x L outputs against the oracle's
+    message-passing ring run on the same full inputs (in place, so the host holds N x S once).
+    With rs_ag, the reduce-scatter and the all-gather of its shards too: shard c must equal
+    chunk c of the all-reduce and the gathered buffers the all-reduce (AG o RS = AR, pinned on
+    the oracle), every element."""
+    es = ELEM_SIZE[dtype]
+    need_gb = (n + 2) * length * es / 2**30
     if _host_ram_gb() < need_gb + 4:
         pytest.skip(f"host RAM below {need_gb + 4:.0f} GB")
     xs = inputs.rank_buffers(n, length, dtype, dist)
@@ -463,24 +485,54 @@ def check_full_size(ra, n, length, dtype, op, dist):
     recvs = [torch.empty_like(s) for s in sends]
     ra.ra_allreduce(sends, recvs, op)
     torch.cuda.synchronize()
-    for r in range(1, n):
-        assert torch.equal(recvs[r].view(torch.uint8), recvs[0].view(torch.uint8)), f"rank {r} differs"
-    idx = sample_indices(length, n)
-    got = to_host(recvs[0][torch.from_numpy(idx).cuda()], dtype)
-    want = oracle.fold_at(xs, op, dtype, idx)
-    assert_same_bits(got, want, dtype, f"sampled n={n} L={length}")
-    del sends, recvs
+    shards = gathered = None
+    if rs_ag:
+        bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+        shards = [torch.empty(e - b, dtype=TORCH_DTYPE[dtype], device="cuda") for b, e in bounds]
+        ra.ra_reduce_scatter(sends, shards, op)
+        del sends
+        gathered = [torch.empty(length, dtype=TORCH_DTYPE[dtype], device="cuda") for _ in range(n)]
+        ra.ra_allgather(shards, gathered)
+        torch.cuda.synchronize()
+    else:
+        del sends
+    want, _, _ = oracle.allreduce(xs, op, dtype, timeout_ms=ORACLE_TIMEOUT_MS, inplace=True)
+    compare_ranks(recvs, want, dtype, f"AR n={n} L={length}")
+    if rs_ag:
+        for c, (b, e) in enumerate(bounds):
+            same_bits_fast(to_host(shards[c], dtype), want[0][b:e], dtype, f"RS n={n} L={length} shard {c}")
+        compare_ranks(gathered, want, dtype, f"AG(RS) n={n} L={length}")
+    del recvs, shards, gathered
     torch.cuda.empty_cache()
 
 
 def test_full_size_n8_f32_avg_64m(ra):
     n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_f32_avg_64m"]
-    check_full_size(ra, n, length, dtype, op, dist)
+    check_full_size(ra, n, length, dtype, op, dist, rs_ag=True)
 
 
 def test_full_size_n8_bf16_avg_gpt2m(ra):
     n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_bf16_avg_gpt2m"]
-    check_full_size(ra, n, length, dtype, op, dist)
+    check_full_size(ra, n, length, dtype, op, dist, rs_ag=True)
+
+
+def test_full_size_n8_bf16_avg_gpt2m_fp32_partials(ra):
+    # the same bucket with fp32 partials, rounded once: every element against the oracle's ring
+    # whose messages are fp32
+    n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_bf16_avg_gpt2m"]
+    if _host_ram_gb() < 2 * n * length * 2 / 2**30 + 6:
+        pytest.skip("host RAM too small for the inputs and the oracle's outputs")
+    xs = inputs.rank_buffers(n, length, dtype, dist)
+    sends = [to_device(x, dtype) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    ra.ra_allreduce_ex(sends, recvs, op, accum="fp32")
+    torch.cuda.synchronize()
+    del sends
+    want, _ = oracle.allreduce_ex(xs, op, dtype, accum="fp32", timeout_ms=ORACLE_TIMEOUT_MS)
+    del xs
+    compare_ranks(recvs, want, dtype, "fp32 partials, full bucket")
+    del recvs
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("n,length", [(n, 1 << p) for n in (8, 16) for p in (8, 10, 12, 14, 16, 18, 20)])
@@ -620,33 +672,21 @@ def test_rabenseifner_rejects_non_power_of_two(ra):
 
 
 @pytest.mark.parametrize("order", ["tree", "rabenseifner"])
-def test_other_orders_full_size_sampled(ra, order):
+def test_other_orders_full_size(ra, order):
+    # the bench workload in tree / Rabenseifner order: every element of every rank against the
+    # oracle's message-passing simulation of that algorithm on the same full inputs
     n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_f32_avg_64m"]
+    if _host_ram_gb() < 2 * n * length * 4 / 2**30 + 6:
+        pytest.skip("host RAM too small for the inputs and the oracle's outputs")
     xs = inputs.rank_buffers(n, length, dtype, dist)
     sends = [to_device(x, dtype) for x in xs]
     recvs = [torch.empty_like(s) for s in sends]
     ra.ra_allreduce_ex(sends, recvs, op, order=order)
     torch.cuda.synchronize()
-    for r in range(1, n):
-        assert torch.equal(recvs[r], recvs[0])
-    idx = sample_indices(length, n, k=1 << 12)
-    got = to_host(recvs[0][torch.from_numpy(idx).cuda()], dtype)
-    # the association depends only on which tree reduces the element (tree: chunks below N/2 use
-    # tree 0), so the sampled columns are evaluated by the oracle laid out in a chunk of the same tree
-    split = (n // 2) * length // n
-    for half, mask in ((0, idx < split), (1, idx >= split)):
-        cols = [np.ascontiguousarray(x[idx][mask]) for x in xs]
-        m = cols[0].size
-        if not m:
-            continue
-        if order == "tree":
-            pad = [np.concatenate([c] * n) for c in cols]  # n chunks of m elements
-            want_all, _ = oracle.allreduce_ex(pad, op, dtype, order=order)
-            want = want_all[0][:m] if half == 0 else want_all[0][(n - 1) * m:]
-        else:
-            want_all, _ = oracle.allreduce_ex(cols, op, dtype, order=order)
-            want = want_all[0]
-        assert_same_bits(got[mask], want, dtype, f"{order} sampled half {half}")
+    del sends
+    want, _ = oracle.allreduce_ex(xs, op, dtype, order=order, timeout_ms=ORACLE_TIMEOUT_MS)
+    del xs
+    compare_ranks(recvs, want, dtype, f"{order} full size")
 
 
 # ---------------------------------------------------------------------------
@@ -722,11 +762,9 @@ def test_bulk_engine_full_size(ra):
     ra.ra_allreduce_ex(sends, recvs, op, engine="bulk", status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
-    for r in range(1, n):
-        assert torch.equal(recvs[r], recvs[0])
-    idx = sample_indices(length, n)
-    got = to_host(recvs[0][torch.from_numpy(idx).cuda()], dtype)
-    assert_same_bits(got, oracle.fold_at(xs, op, dtype, idx), dtype, "bulk full size sampled")
+    del sends
+    want, _, _ = oracle.allreduce(xs, op, dtype, timeout_ms=ORACLE_TIMEOUT_MS, inplace=True)
+    compare_ranks(recvs, want, dtype, "bulk full size")
 
 
 def test_bulk_wait_runs_out_and_reports(ra):
@@ -746,3 +784,28 @@ def test_bulk_wait_runs_out_and_reports(ra):
     torch.cuda.synchronize()
     assert status.item() == 0
     assert_same_bits(to_host(recvs[1], "f32"), want[1], "f32", "after the self-test")
+
+
+def test_bulk_wait_reports_in_the_withheld_chunks_word(ra):
+    # per-chunk status words (the layout of the no-alloc entry point): chunk c's first tile is
+    # withheld, so word c alone turns nonzero; every other chunk finishes and reports 0
+    n, length, c = 4, 4 * 1024 * 8, 2
+    xs = inputs.rank_buffers(n, length, "f32", ("normal", 1.0), seed_base=5)
+    sends = [to_device(x, "f32") for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    words = torch.zeros(n, dtype=torch.int32, device="cuda")
+    ra.ra_selftest_bulk_timeout(sends, recvs, words, withhold_chunk=c, per_chunk=True)
+    torch.cuda.synchronize()
+    codes = words.cpu().tolist()
+    assert codes[c] in (1, 2) and all(codes[k] == 0 for k in range(n) if k != c), codes
+    want, _, _ = oracle.allreduce(xs, "sum", "f32")
+    for k in range(n):  # the chunks that finished hold their results
+        if k == c:
+            continue
+        b, e = oracle.chunk_range(length, n, k)
+        assert_same_bits(to_host(recvs[0], "f32")[b:e], want[0][b:e], "f32", f"chunk {k} beside the withheld one")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ra.ra_allreduce_ex(sends, recvs, "sum", engine="bulk", status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert_same_bits(to_host(recvs[3], "f32"), want[3], "f32", "after the self-test")
