@@ -18,6 +18,7 @@ cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid,
 cudaError_t launch_ordered_kernel(bool is_rs, int dtype, int op, const OrderArgs& o, dim3 grid, cudaStream_t s);
 cudaError_t launch_bulk_kernel(int dtype, int op, const BulkArgs& b, dim3 grid, size_t smem, cudaStream_t s);
 cudaError_t configure_bulk_kernel(int dtype, int op, size_t smem);
+cudaError_t launch_group_kernel(int dtype, int op, const GroupArgs& g, dim3 grid, cudaStream_t s);
 }  // namespace ra
 
 namespace {
@@ -532,6 +533,37 @@ ra_status_t bucket_plan(const size_t* counts, int nparams, size_t bucket_bytes, 
   return nb <= max_buckets ? RA_SUCCESS : RA_ERR_INVALID_ARG;
 }
 
+// The all-reduces of buckets [first, first + k) of the table in one launch (k >= 2):
+// ring order, register engine; `whole` holds the checked N whole buffers.
+ra_status_t launch_group(const ra::Args& whole, int dtype, int op, int accum, int max_sms, const size_t* bucket_begin,
+                         const size_t* bucket_count, const int* members, int k, void* stream) {
+  ra::GroupArgs g;
+  g.a = whole;
+  g.nbuckets = (uint32_t)k;
+  uint64_t total = 0;
+  for (int i = 0; i < k; ++i) {
+    g.begin[i] = bucket_begin[members[i]];
+    g.count[i] = bucket_count[members[i]];
+    total += g.count[i];
+  }
+  ra::Args& a = g.a;
+  a.acc32 = (accum == RA_ACCUM_FP32 && (dtype == RA_FLOAT16 || dtype == RA_BFLOAT16) && op != RA_MIN &&
+             op != RA_MAX)
+                ? 1
+                : 0;
+  a.shape = shape_for(a.nranks, false, a.acc32 != 0, dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
+                      op == RA_MIN || op == RA_MAX);
+  // the bucket loop needs a few more registers than ShapeS and ShapeM3 budget (a shape
+  // changes how fast, never which bits)
+  if (a.shape == ra::SHAPE_S || a.shape == ra::SHAPE_M3) a.shape = ra::SHAPE_M;
+  a.count = total;  // sizes the grid like one all-reduce of the group's elements
+  dim3 grid;
+  const ra_status_t st = grid_for(a, dtype, a.shape, max_sms, &grid);
+  if (st != RA_SUCCESS) return st;
+  const cudaError_t err = ra::launch_group_kernel(dtype, op, g, grid, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
+}
+
 ra_status_t run_buckets(const void* const* sendbufs, void* const* recvbufs, size_t count, ra_dtype_t dtype,
                         ra_op_t op, int nranks, int nbuckets, const size_t* bucket_begin,
                         const size_t* bucket_count, void* const* ready_events, const ra_options_t* options,
@@ -553,25 +585,56 @@ ra_status_t run_buckets(const void* const* sendbufs, void* const* recvbufs, size
       dir = d;
     }
   }
+  if (options == nullptr) options = &kDefaultOptions;
+  // the per-bucket path checks the options; the grouped one takes the defaults' engine and order only
+  const bool groupable = count > 0 && options->engine == RA_ENGINE_REGISTERS && options->order == RA_ORDER_RING &&
+                         (options->accum == RA_ACCUM_DTYPE || options->accum == RA_ACCUM_FP32) &&
+                         options->max_sms >= 0;
   const int es = elem_size(dtype);
   const void* s_ptr[RA_MAX_RANKS];
   void* d_ptr[RA_MAX_RANKS];
-  for (int b = 0; b < nbuckets; ++b) {
-    if (ready_events && ready_events[b]) {
-      const cudaError_t err = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream),
-                                                  static_cast<cudaEvent_t>(ready_events[b]), 0);
-      if (err != cudaSuccess) return cuda_failed(err);
-    }
-    if (bucket_count[b] == 0) continue;
+  auto one_bucket = [&](int b) -> ra_status_t {
     const size_t off = bucket_begin[b] * (size_t)es;
     for (int r = 0; r < nranks; ++r) {
       s_ptr[r] = static_cast<const char*>(sendbufs[r]) + off;
       d_ptr[r] = static_cast<char*>(recvbufs[r]) + off;
     }
-    st = run(ra::KIND_ALLREDUCE, s_ptr, d_ptr, bucket_count[b], dtype, op, nranks, stream, options);
-    if (st != RA_SUCCESS) return st;
+    return run(ra::KIND_ALLREDUCE, s_ptr, d_ptr, bucket_count[b], dtype, op, nranks, stream, options);
+  };
+  // Buckets with no ready event of their own follow the previous bucket without a
+  // wait; a run of such buckets goes out as one grouped launch.
+  int members[ra::kMaxGroup];
+  int k = 0;
+  auto flush = [&]() -> ra_status_t {
+    ra_status_t r = RA_SUCCESS;
+    if (k == 1) r = one_bucket(members[0]);
+    else if (k > 1)
+      r = launch_group(whole, dtype, op, options->accum, options->max_sms, bucket_begin, bucket_count, members, k,
+                       stream);
+    k = 0;
+    return r;
+  };
+  for (int b = 0; b < nbuckets; ++b) {
+    if (ready_events && ready_events[b]) {
+      st = flush();
+      if (st != RA_SUCCESS) return st;
+      const cudaError_t err = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream),
+                                                  static_cast<cudaEvent_t>(ready_events[b]), 0);
+      if (err != cudaSuccess) return cuda_failed(err);
+    }
+    if (bucket_count[b] == 0) continue;
+    if (!groupable) {
+      st = one_bucket(b);
+      if (st != RA_SUCCESS) return st;
+      continue;
+    }
+    members[k++] = b;
+    if (k == ra::kMaxGroup) {
+      st = flush();
+      if (st != RA_SUCCESS) return st;
+    }
   }
-  return RA_SUCCESS;
+  return flush();
 }
 
 }  // namespace

@@ -47,10 +47,18 @@ namespace ra {
 // sum/avg/prod at 8 CTAs/SM (97-98%, against 88% at 6); from N = 4 sum/avg
 // keep batches of 4 (96-102%) and min/max take 128 x 2 with batches of 2
 // (96-103%, against 91-99%).
-// 0: the CTAs of a chunk interleave (grid-stride); 1: each CTA streams one
-// contiguous slab of the chunk.
+// How a chunk's vectors are dealt to the CTAs of its row. Every warp moves 32
+// consecutive vectors (1 KB with 32-byte vectors) per unroll slot and trip.
+//  0: grid-stride by CTA: trip k of CTA x covers the CTA-sized block x of the
+//     trip; the last, partial trip then falls on the row's first CTAs only.
+//     Since CTA x of every chunk lands on the same SM, those SMs run it while
+//     the rest idle.
+//  1: each CTA streams one contiguous slab of the chunk.
+//  2: grid-stride by warp: the warps of a trip are dealt across the row's CTAs
+//     (warp slot s of CTA x takes block s * gridDim.x + x), so the partial last
+//     trip is spread over every CTA, and every SM, of the row.
 #ifndef RA_SCHEDULE
-#define RA_SCHEDULE 0
+#define RA_SCHEDULE 2
 #endif
 
 // Programmatic dependent launch. With RA_PDL set (the default), the
@@ -179,23 +187,41 @@ struct Args {
   int shape;   // ShapeId of the fused AR/RS launch
 };
 
-// The vectors [jbeg, jend) of a chunk this CTA handles, visited by its threads
-// from jbeg + threadIdx.x in strides of jstride (kUnroll vectors kThreads apart
-// per trip).
-struct Span {
-  uint64_t jbeg, jend, jstride;
+// The walk of one CTA over a chunk's nv vectors: trip bases run over
+// [begin, end) in steps of stride; in each trip this warp takes the 32
+// vectors base + slot0 + u * uslot + lane (u < kUnroll); vectors at or past
+// `end` are skipped. Trip bases are the same for every thread of the CTA.
+struct Walk {
+  uint64_t begin, end, stride;
+  uint32_t slot0, uslot;  // offsets inside one trip (less than stride)
 };
 template <class SH>
-__device__ __forceinline__ Span cta_span(uint64_t nv) {
-  constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
-#if RA_SCHEDULE == 0
-  return {(uint64_t)blockIdx.x * kThreads * kUnroll, nv, (uint64_t)gridDim.x * kThreads * kUnroll};
-#else
+__device__ __forceinline__ Walk cta_walk(uint64_t nv) {
+  constexpr uint32_t kThreads = SH::kThreads, kUnroll = SH::kUnroll, kWarps = kThreads / 32;
+  const uint32_t wid = threadIdx.x / 32;
+  Walk w;
+#if RA_SCHEDULE == 1
   const uint64_t trip = (uint64_t)kThreads * kUnroll;
   const uint64_t per = ((nv + gridDim.x - 1) / gridDim.x + trip - 1) / trip * trip;
-  const uint64_t b = (uint64_t)blockIdx.x * per;
-  return {b, b + per < nv ? b + per : nv, trip};
+  w.begin = (uint64_t)blockIdx.x * per;
+  w.end = w.begin + per < nv ? w.begin + per : nv;
+  w.stride = trip;
+  w.slot0 = wid * 32;
+  w.uslot = kThreads;
+#elif RA_SCHEDULE == 2
+  w.begin = 0;
+  w.end = nv;
+  w.stride = (uint64_t)gridDim.x * kThreads * kUnroll;
+  w.slot0 = (wid * gridDim.x + blockIdx.x) * 32;
+  w.uslot = kWarps * gridDim.x * 32;
+#else
+  w.begin = 0;
+  w.end = nv;
+  w.stride = (uint64_t)gridDim.x * kThreads * kUnroll;
+  w.slot0 = blockIdx.x * kThreads * kUnroll + wid * 32;
+  w.uslot = kThreads;
 #endif
+  return w;
 }
 
 // ---------------------------------------------------------------------------
@@ -340,24 +366,24 @@ __device__ __forceinline__ void for_each_edge_elem(uint64_t b0, uint64_t vb, uin
 // ---------------------------------------------------------------------------
 // all-reduce: every destination receives the fold
 // ---------------------------------------------------------------------------
+// The all-reduce of the element range [b0, b1), one chunk of one collective,
+// folded in ring order from rank c: whole vectors, then the edge elements.
 template <int DT, int OP, bool ACC32, class SH>
-__global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(const __grid_constant__ Args a) {
-  pdl_enter();
+__device__ __forceinline__ void ar_range(const Args& a, int c, int n, uint64_t b0, uint64_t b1) {
   constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
-  const int n = a.nranks, c = blockIdx.y;
-  const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
-  const Span sp = cta_span<SH>((ve - vb) / V);
-  for (uint64_t j0 = sp.jbeg + threadIdx.x; j0 < sp.jend; j0 += sp.jstride) {
+  const Walk w = cta_walk<SH>((ve - vb) / V);
+  // a thread's first vector of each trip; its later unroll slots lie further on
+  for (uint64_t j0 = w.begin + w.slot0 + (threadIdx.x & 31u); j0 < w.end; j0 += w.stride) {
     uint64_t off[kUnroll];
     bool ok[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint64_t j = j0 + (uint64_t)u * kThreads;
-      ok[u] = j < sp.jend;
+      const uint64_t j = j0 + (uint64_t)u * w.uslot;
+      ok[u] = j < w.end;
       off[u] = (vb + j * V) * ES;
     }
     Vec acc[kUnroll];
@@ -375,6 +401,41 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(
   });
 }
 
+template <int DT, int OP, bool ACC32, class SH>
+__global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(const __grid_constant__ Args a) {
+  pdl_enter();
+  const int n = a.nranks, c = blockIdx.y;
+  ar_range<DT, OP, ACC32, SH>(a, c, n, chunk_begin(c, n, a.count), chunk_begin(c + 1, n, a.count));
+}
+
+// ---------------------------------------------------------------------------
+// grouped all-reduce: several independent all-reduces of element ranges of the
+// same N buffers in one launch (gradient buckets that need no wait between
+// them). Bucket b is the all-reduce of elements [begin[b], begin[b] + count[b])
+// with its own chunk bounds, so each bucket's bits are those of a launch of its
+// own. Row c of CTAs folds chunk c of every bucket in turn; a CTA goes on to
+// the next bucket as soon as its share of one is done, so the buckets' partial
+// last trips overlap instead of each paying a launch's ramp and tail.
+// ---------------------------------------------------------------------------
+constexpr int kMaxGroup = 64;
+struct GroupArgs {
+  Args a;             // the N whole buffers; a.count = the group's total elements
+  uint32_t nbuckets;  // 1..kMaxGroup
+  uint64_t begin[kMaxGroup];
+  uint64_t count[kMaxGroup];
+};
+
+template <int DT, int OP, bool ACC32, class SH>
+__global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_group_kernel(const __grid_constant__ GroupArgs g) {
+  pdl_enter();
+  const Args& a = g.a;
+  const int n = a.nranks, c = blockIdx.y;
+  for (uint32_t b = 0; b < g.nbuckets; ++b) {
+    const uint64_t at = g.begin[b], len = g.count[b];
+    ar_range<DT, OP, ACC32, SH>(a, c, n, at + chunk_begin(c, n, len), at + chunk_begin(c + 1, n, len));
+  }
+}
+
 // ---------------------------------------------------------------------------
 // reduce-scatter: chunk c's fold goes to dst[c], compact (element i -> i - b0)
 // ---------------------------------------------------------------------------
@@ -388,7 +449,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
-  const Span sp = cta_span<SH>((ve - vb) / V);
+  const Walk w = cta_walk<SH>((ve - vb) / V);
   void* out = a.dst[c];
   const bool out_vec = (a.compact_aligned >> c) & 1u;
   // Off the vector grid the plain kernel stores each lane's vector in 4-byte
@@ -398,15 +459,14 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
   // 2-byte units, so each warp store covers 64 contiguous bytes.
   __shared__ Vec stage[OFFGRID ? kThreads : 1];
   const uint32_t lane = threadIdx.x & 31u, wfirst = threadIdx.x & ~31u;
-  // warp-uniform trips (the warp synchronises on the off-grid path)
-  for (uint64_t jw0 = sp.jbeg + wfirst; jw0 < sp.jend; jw0 += sp.jstride) {
-    const uint64_t j0 = jw0 + lane;
+  // trips are warp-uniform (the warp synchronises on the off-grid path)
+  for (uint64_t base = w.begin; base < w.end; base += w.stride) {
     uint64_t off[kUnroll];
     bool ok[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint64_t j = j0 + (uint64_t)u * kThreads;
-      ok[u] = j < sp.jend;
+      const uint64_t j = base + w.slot0 + (uint64_t)u * w.uslot + lane;
+      ok[u] = j < w.end;
       off[u] = (vb + j * V) * ES;
     }
     Vec acc[kUnroll];
@@ -416,12 +476,12 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
       if (out_vec) {
         if (ok[u]) st_vec(static_cast<char*>(out) + off[u] - b0 * ES, acc[u]);
       } else if constexpr (OFFGRID) {
-        const uint64_t jw = jw0 + (uint64_t)u * kThreads;  // the warp's first vector this trip
+        const uint64_t jw = base + w.slot0 + (uint64_t)u * w.uslot;  // the warp's first vector this trip
         char* wdst = static_cast<char*>(out) + (vb + jw * V - b0) * ES;
         if ((reinterpret_cast<uintptr_t>(wdst) & 3u) == 0) {  // the chunk allows 4-byte units
           if (ok[u]) st_vec_units(static_cast<char*>(out) + off[u] - b0 * ES, acc[u]);
         } else {  // 2-byte units: the warp's results go out through shared memory, lanes on consecutive units
-          const uint32_t bytes = (jw >= sp.jend ? 0u : (sp.jend - jw < 32 ? (uint32_t)(sp.jend - jw) : 32u)) * kVecBytes;
+          const uint32_t bytes = (jw >= w.end ? 0u : (w.end - jw < 32 ? (uint32_t)(w.end - jw) : 32u)) * kVecBytes;
           stage[threadIdx.x] = acc[u];
           __syncwarp();
           const char* sw = reinterpret_cast<const char*>(stage + wfirst);
@@ -452,17 +512,17 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ag_copy_kernel(c
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
-  const Span sp = cta_span<SH>((ve - vb) / V);
+  const Walk w = cta_walk<SH>((ve - vb) / V);
   const void* in = a.src[c];
   const bool in_vec = (a.compact_aligned >> c) & 1u;
-  for (uint64_t j0 = sp.jbeg + threadIdx.x; j0 < sp.jend; j0 += sp.jstride) {
+  for (uint64_t j0 = w.begin + w.slot0 + (threadIdx.x & 31u); j0 < w.end; j0 += w.stride) {
     uint64_t off[kUnroll];
     bool ok[kUnroll];
     Vec v[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint64_t j = j0 + (uint64_t)u * kThreads;
-      ok[u] = j < sp.jend;
+      const uint64_t j = j0 + (uint64_t)u * w.uslot;
+      ok[u] = j < w.end;
       off[u] = (vb + j * V) * ES;
       if (!ok[u]) continue;
       if (in_vec) {
@@ -508,6 +568,44 @@ cudaError_t launch_fused_shape(int kind, const Args& a, dim3 grid, cudaStream_t 
   return kind == KIND_ALLREDUCE ? launch_ar<DT, OP, ACC32, SH>(a, grid, s) : launch_rs<DT, OP, ACC32, SH>(a, grid, s);
 }
 
+template <int DT, int OP, bool ACC32, class SH>
+cudaError_t launch_group_shape(const GroupArgs& g, dim3 grid, cudaStream_t s) {
+  return launch_programmatic(ar_group_kernel<DT, OP, ACC32, SH>, grid, SH::kThreads, 0, s, g);
+}
+
+// The grouped all-reduce on the all-reduce shapes shape_for() can choose, but
+// for the two whose register budget the bucket loop would overflow (ShapeS,
+// ShapeM3): the planner sends those groups to ShapeM.
+template <int DT, int OP, bool ACC32>
+cudaError_t launch_group_fused(const GroupArgs& g, dim3 grid, cudaStream_t s) {
+  switch (g.a.shape) {
+    case SHAPE_S4:
+      if constexpr (!ACC32) return launch_group_shape<DT, OP, false, ShapeS4>(g, grid, s);
+      break;
+    case SHAPE_N3:
+      if constexpr (!ACC32 && Elem<DT>::kSize == 4) return launch_group_shape<DT, OP, false, ShapeN3>(g, grid, s);
+      break;
+    case SHAPE_M: return launch_group_shape<DT, OP, ACC32, ShapeM>(g, grid, s);
+    case SHAPE_W: return launch_group_shape<DT, OP, ACC32, ShapeW>(g, grid, s);
+    case SHAPE_MB8:
+      if constexpr (!ACC32 && (DT == DT_F16 || DT == DT_BF16) && OP != OP_MIN && OP != OP_MAX)
+        return launch_group_shape<DT, OP, false, ShapeMB8>(g, grid, s);
+      break;
+    case SHAPE_W8: return launch_group_shape<DT, OP, ACC32, ShapeW8>(g, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int DT, int OP>
+cudaError_t launch_group_op(const GroupArgs& g, dim3 grid, cudaStream_t s) {
+  constexpr bool kPartials = (DT == DT_F16 || DT == DT_BF16) && OP != OP_MIN && OP != OP_MAX;
+  if constexpr (kPartials) {
+    if (g.a.acc32) return launch_group_fused<DT, OP, true>(g, grid, s);
+  }
+  if (g.a.acc32) return cudaErrorInvalidValue;
+  return launch_group_fused<DT, OP, false>(g, grid, s);
+}
+
 // Only the (kind, accumulation, shape) combinations shape_for() can choose are
 // instantiated; any other is refused.
 template <int DT, int OP, bool ACC32>
@@ -540,8 +638,8 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (rs) return launch_rs<DT, OP, false, ShapeRS>(a, grid, s);
       }
       break;
-    case SHAPE_N3:
-      if constexpr (!ACC32) {
+    case SHAPE_N3:  // 4-byte types only: fp16/bf16 take ShapeM3 at N = 3
+      if constexpr (!ACC32 && Elem<DT>::kSize == 4) {
         if (!rs) return launch_ar<DT, OP, false, ShapeN3>(a, grid, s);
       }
       break;

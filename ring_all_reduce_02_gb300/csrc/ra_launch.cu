@@ -12,7 +12,8 @@ namespace ra {
   cudaError_t launch_slice_##DT##_##OP(int kind, const Args& a, dim3 grid, cudaStream_t s);       \
   cudaError_t launch_ordered_slice_##DT##_##OP(bool is_rs, const OrderArgs& o, dim3 grid, cudaStream_t s); \
   cudaError_t launch_bulk_slice_##DT##_##OP(const BulkArgs& b, dim3 grid, size_t smem, cudaStream_t s); \
-  cudaError_t configure_bulk_slice_##DT##_##OP(size_t smem);
+  cudaError_t configure_bulk_slice_##DT##_##OP(size_t smem); \
+  cudaError_t launch_group_slice_##DT##_##OP(const GroupArgs& g, dim3 grid, cudaStream_t s);
 #define RA_DECLARE_DT(DT) \
   RA_DECLARE_SLICE(DT, 0) RA_DECLARE_SLICE(DT, 1) RA_DECLARE_SLICE(DT, 2) RA_DECLARE_SLICE(DT, 3) RA_DECLARE_SLICE(DT, 4)
 RA_DECLARE_DT(0)
@@ -34,10 +35,15 @@ using OrderedSliceFn = cudaError_t (*)(bool, const OrderArgs&, dim3, cudaStream_
    configure_bulk_slice_##DT##_3, configure_bulk_slice_##DT##_4}
 using BulkSliceFn = cudaError_t (*)(const BulkArgs&, dim3, size_t, cudaStream_t);
 using BulkConfigureFn = cudaError_t (*)(size_t);
+#define RA_GROW(DT)                                                                            \
+  {launch_group_slice_##DT##_0, launch_group_slice_##DT##_1, launch_group_slice_##DT##_2, \
+   launch_group_slice_##DT##_3, launch_group_slice_##DT##_4}
+using GroupSliceFn = cudaError_t (*)(const GroupArgs&, dim3, cudaStream_t);
 const SliceFn kSlices[4][5] = {RA_ROW(0), RA_ROW(1), RA_ROW(2), RA_ROW(3)};
 const OrderedSliceFn kOrderedSlices[4][5] = {RA_OROW(0), RA_OROW(1), RA_OROW(2), RA_OROW(3)};
 const BulkSliceFn kBulkSlices[4][5] = {RA_BROW(0), RA_BROW(1), RA_BROW(2), RA_BROW(3)};
 const BulkConfigureFn kBulkConfigure[4][5] = {RA_CROW(0), RA_CROW(1), RA_CROW(2), RA_CROW(3)};
+const GroupSliceFn kGroupSlices[4][5] = {RA_GROW(0), RA_GROW(1), RA_GROW(2), RA_GROW(3)};
 
 template <int DT, int kUnroll>
 cudaError_t launch_ag_tma(const Args& a, dim3 grid, cudaStream_t s) {
@@ -91,6 +97,11 @@ cudaError_t launch_kernel(int kind, int dtype, int op, const Args& a, dim3 grid,
 cudaError_t launch_ordered_kernel(bool is_rs, int dtype, int op, const OrderArgs& o, dim3 grid, cudaStream_t s) {
   if (dtype < 0 || dtype > 3 || op < 0 || op > 4) return cudaErrorInvalidValue;
   return kOrderedSlices[dtype][op](is_rs, o, grid, s);
+}
+
+cudaError_t launch_group_kernel(int dtype, int op, const GroupArgs& g, dim3 grid, cudaStream_t s) {
+  if (dtype < 0 || dtype > 3 || op < 0 || op > 4) return cudaErrorInvalidValue;
+  return kGroupSlices[dtype][op](g, grid, s);
 }
 
 cudaError_t configure_bulk_kernel(int dtype, int op, size_t smem) {

@@ -29,4 +29,7 @@ cudaError_t RA_CAT3(launch_bulk_slice, RA_SLICE_DT, RA_SLICE_OP)(const BulkArgs&
 cudaError_t RA_CAT3(configure_bulk_slice, RA_SLICE_DT, RA_SLICE_OP)(size_t smem) {
   return configure_bulk_op<RA_SLICE_DT, RA_SLICE_OP>(smem);
 }
+cudaError_t RA_CAT3(launch_group_slice, RA_SLICE_DT, RA_SLICE_OP)(const GroupArgs& g, dim3 grid, cudaStream_t s) {
+  return launch_group_op<RA_SLICE_DT, RA_SLICE_OP>(g, grid, s);
+}
 }  // namespace ra

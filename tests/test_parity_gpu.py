@@ -719,6 +719,91 @@ def test_bucketed_allreduce(ra, dtype, op):
             assert_same_bits(to_host(recvs[r][b:b + c], dtype), want[r], dtype, f"bucket {b} rank {r}")
 
 
+def _bucket_want(xs, b, c, op, dtype, accum):
+    part = [np.ascontiguousarray(x[b:b + c]) for x in xs]
+    if accum == "fp32":
+        return oracle.allreduce_ex(part, op, dtype, accum="fp32")[0]
+    return oracle.allreduce(part, op, dtype)[0]
+
+
+@pytest.mark.parametrize("dtype,op,accum", [("f32", "sum", "dtype"), ("bf16", "avg", "dtype"), ("bf16", "avg", "fp32"),
+                                            ("i32", "max", "dtype"), ("f16", "prod", "dtype"), ("f32", "avg", "dtype")])
+def test_grouped_buckets(ra, dtype, op, accum):
+    # buckets that need no wait between them go out as one grouped launch; a ready event on a
+    # bucket starts a new group. Every bucket must equal its own all-reduce (own chunk bounds).
+    counts = [1000, 3, 77, 4096, 10, 2048, 5, 65536, 1, 333, 70001, 12345, 7]
+    es = ELEM_SIZE[dtype]
+    plan = ra.ra_bucket_plan(counts, 5000 * es, es)
+    length = sum(counts)
+    for n in (1, 2, 3, 5, 6, 8, 16):
+        xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=31 + n)
+        for every in (0, 3):  # 0: no events (one group); 3: an event on every third bucket
+            sends = [to_device(x, dtype) for x in xs]
+            recvs = [torch.zeros_like(s) for s in sends]
+            events = None
+            if every:
+                events = []
+                for k in range(len(plan)):
+                    ev = None
+                    if k % every == 0:
+                        ev = torch.cuda.Event()
+                        ev.record()
+                    events.append(ev)
+            ra.ra_allreduce_buckets(sends, recvs, plan, op, ready_events=events, accum=accum)
+            torch.cuda.synchronize()
+            for b, c in plan:
+                want = _bucket_want(xs, b, c, op, dtype, accum)
+                for r in range(n):
+                    assert_same_bits(to_host(recvs[r][b:b + c], dtype), want[r], dtype,
+                                     f"n={n} every={every} bucket {b}+{c} rank {r}")
+
+
+def test_grouped_buckets_many_and_empty(ra):
+    # more buckets than one grouped launch holds (so the group is split), zero-length buckets, in
+    # place, and ascending order
+    n, dtype, op = 4, "f32", "sum"
+    sizes = [(k * 37) % 211 for k in range(150)]  # includes zeros
+    begins, at = [], 0
+    for c in sizes:
+        begins.append(at)
+        at += c
+    length = at
+    plan = list(zip(begins, sizes))
+    xs = inputs.rank_buffers(n, length, dtype, ("uniform", -1.0, 1.0), seed_base=5)
+    sends = [to_device(x, dtype) for x in xs]
+    ra.ra_allreduce_buckets(sends, sends, plan, op)
+    torch.cuda.synchronize()
+    for b, c in plan:
+        if c == 0:
+            continue
+        want = _bucket_want(xs, b, c, op, dtype, "dtype")
+        for r in range(n):
+            assert_same_bits(to_host(sends[r][b:b + c], dtype), want[r], dtype, f"bucket {b}+{c} rank {r}")
+
+
+def test_grouped_buckets_full_size_gpt2m(ra):
+    # the 33 DDP buckets (25 MB cap) of the bf16 GPT-2-medium gradient, no ready events: grouped
+    # launches; every element of every bucket against the oracle's ring run on that bucket
+    n, length, dtype, op, dist = inputs.WORKLOADS["ar_n8_bf16_avg_gpt2m"]
+    counts = [int(np.prod(s)) for _, s in inputs.gpt2_medium_param_shapes()]
+    plan = ra.ra_bucket_plan(counts, 25 * 1000 * 1000, 2)
+    assert len(plan) == 33
+    if _host_ram_gb() < 2 * n * length * 2 / 2**30 + 6:
+        pytest.skip("host RAM too small")
+    xs = inputs.rank_buffers(n, length, dtype, dist)
+    sends = [to_device(x, dtype) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    ra.ra_allreduce_buckets(sends, recvs, plan, op)
+    torch.cuda.synchronize()
+    del sends
+    got = [to_host(r, dtype) for r in recvs]
+    del recvs
+    for b, c in plan:
+        want = _bucket_want(xs, b, c, op, dtype, "dtype")
+        for r in range(n):
+            same_bits_fast(got[r][b:b + c], want[r], dtype, f"bucket {b}+{c} rank {r}")
+
+
 def test_sm_budget_changes_nothing_but_speed(ra):
     n, length = 8, (1 << 22) + 5
     xs = inputs.rank_buffers(n, length, "bf16", ("normal", 1.0), seed_base=4)
