@@ -220,13 +220,28 @@ ra_status_t sm_budget(int max_sms, int* sms) {
 
 // Grid: blockIdx.y = chunk (or rank, for the ring steps); blockIdx.x = CTAs
 // sharing it, enough to cover its vectors but no more than one resident wave
-// of the launch shape on the SM budget.
+// of the launch shape on the SM budget (RA_ONE_WAVE, a build-time tunable:
+// 0 lets the fused kernels take one CTA per trip instead).
+#ifndef RA_ONE_WAVE
+#define RA_ONE_WAVE 1
+#endif
 ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3* grid) {
   int threads, per_thread, min_blocks, sms = 0;
-  if (shape >= ra::kShapeAgBase) {
+  if (shape == ra::kShapeAgBase + ra::AG_TILE) {
+    // one CTA per whole tile of the longest chunk, plus one per chunk for its leftovers
     const ra::AgPlan p = ra::ag_plan_for(a.nranks);
-    threads = ra::kAgThreads, min_blocks = p.blocks_per_sm;
-    per_thread = p.kernel != ra::AG_REGISTERS ? p.unroll : ra::AgShape::kUnroll;
+    const int v = ra::kVecBytes / elem_size(dtype);
+    const uint64_t gx = p.unroll == 1 ? ra::ag_tile_grid_x<1>(a.count, a.nranks, v)
+                                      : (p.unroll == 2 ? ra::ag_tile_grid_x<2>(a.count, a.nranks, v)
+                                                       : ra::ag_tile_grid_x<4>(a.count, a.nranks, v));
+    if (gx > 0x7fffffffull) return RA_ERR_UNSUPPORTED;
+    *grid = dim3((unsigned)gx, (unsigned)a.nranks);
+    return RA_SUCCESS;
+  }
+  if (shape >= ra::kShapeAgBase) {  // the register all-gather
+    const ra::AgPlan p = ra::ag_plan_for(a.nranks);
+    threads = ra::AgShape::kThreads, per_thread = ra::AgShape::kUnroll;
+    min_blocks = p.kernel == ra::AG_REGISTERS ? p.blocks_per_sm : ra::AgShape::kMinBlocks;
   } else if (shape == ra::SHAPE_STEP) {
     threads = ra::StepShape::kThreads, per_thread = ra::StepShape::kUnroll, min_blocks = ra::StepShape::kMinBlocks;
   } else {
@@ -236,21 +251,19 @@ ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3*
   if (st != RA_SUCCESS) return st;
   const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
   const uint64_t n = (uint64_t)a.nranks;
-  if (shape == ra::kShapeAgBase + ra::AG_TMA_FLAT) {  // one row of CTAs shared by all chunks
-    const uint64_t tiles = n * (per_thread == 2 ? ra::ag_tiles_per_chunk_bound<2>(a.count, a.nranks, (int)v)
-                                                : ra::ag_tiles_per_chunk_bound<1>(a.count, a.nranks, (int)v));
-    uint64_t gx = (uint64_t)sms * min_blocks;
-    if (gx > tiles) gx = tiles;
-    if (gx < 1) gx = 1;
-    *grid = dim3((unsigned)gx, 1);
-    return RA_SUCCESS;
-  }
   const uint64_t per_chunk = (a.count + n - 1) / n;
   const uint64_t work = a.vec_ok ? (per_chunk / v + 1) : per_chunk;  // vectors, or elements
   const uint64_t per_cta = a.vec_ok ? (uint64_t)threads * per_thread : (uint64_t)threads;
   uint64_t gx = (work + per_cta - 1) / per_cta;
   const uint64_t cap = (uint64_t)sms * min_blocks / n;
+#if RA_ONE_WAVE
   if (gx > cap) gx = cap;
+#else  // tuning sweeps: as many CTAs as trips of the shape (each CTA makes one trip)
+  if (shape >= ra::kShapeAgBase || shape == ra::SHAPE_STEP || max_sms > 0) {
+    if (gx > cap) gx = cap;
+  }
+  if (gx > 0x7fffffffull) return RA_ERR_UNSUPPORTED;
+#endif
   if (gx < 1) gx = 1;
   *grid = dim3((unsigned)gx, (unsigned)a.nranks);
   return RA_SUCCESS;
@@ -447,11 +460,11 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
              op != RA_MAX)
                 ? 1
                 : 0;
-  // the flat all-gather deals whole tiles to the SMs and gives each chunk's
-  // per-element work to one CTA: with mixed address phases (every element on
-  // the per-element path) the rows of CTAs per chunk spread it instead
+  // the tile all-gather gives a chunk's per-element work to one CTA: with mixed
+  // address phases (every element on the per-element path) the register
+  // kernel's rows of CTAs spread it instead
   int ag_kernel = ra::ag_plan_for(nranks).kernel;
-  if (ag_kernel == ra::AG_TMA_FLAT && !a.vec_ok) ag_kernel = ra::AG_TMA_STORE;
+  if (!a.vec_ok) ag_kernel = ra::AG_REGISTERS;
   a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ag_kernel
                                        : shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
                                                    dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,

@@ -46,36 +46,24 @@ const BulkConfigureFn kBulkConfigure[4][5] = {RA_CROW(0), RA_CROW(1), RA_CROW(2)
 const GroupSliceFn kGroupSlices[4][5] = {RA_GROW(0), RA_GROW(1), RA_GROW(2), RA_GROW(3)};
 
 template <int DT, int kUnroll>
-cudaError_t launch_ag_tma(const Args& a, dim3 grid, cudaStream_t s) {
-  constexpr uint32_t smem = kAgStages * ag_tile_bytes<kUnroll>();
+cudaError_t launch_ag_tile(const Args& a, dim3 grid, cudaStream_t s) {
+  constexpr uint32_t smem = ag_tile_bytes<kUnroll>();
   if constexpr (smem > 48 * 1024) {  // above the default limit of dynamic shared memory
     const cudaError_t err =
-        cudaFuncSetAttribute(ag_tma_store_kernel<DT, kUnroll>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(ag_tile_kernel<DT, kUnroll>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }
-  return launch_programmatic(ag_tma_store_kernel<DT, kUnroll>, grid, kAgThreads, smem, s, a);
-}
-
-template <int DT, int kUnroll>
-cudaError_t launch_ag_flat(const Args& a, dim3 grid, cudaStream_t s) {
-  constexpr uint32_t smem = kAgStages * ag_tile_bytes<kUnroll>();
-  if constexpr (smem > 48 * 1024) {
-    const cudaError_t err =
-        cudaFuncSetAttribute(ag_tma_flat_kernel<DT, kUnroll>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
-  return launch_programmatic(ag_tma_flat_kernel<DT, kUnroll>, grid, kAgThreads, smem, s, a);
+  return launch_programmatic(ag_tile_kernel<DT, kUnroll>, grid, kAgThreads, smem, s, a);
 }
 
 template <int DT>
 cudaError_t launch_op_free(int kind, const Args& a, dim3 grid, cudaStream_t s) {
-  if (kind == KIND_ALLGATHER && a.shape == kShapeAgBase + AG_TMA_STORE) {
-    if (ag_plan_for(a.nranks).unroll == 2) return launch_ag_tma<DT, 2>(a, grid, s);
-    return launch_ag_tma<DT, 1>(a, grid, s);
-  }
-  if (kind == KIND_ALLGATHER && a.shape == kShapeAgBase + AG_TMA_FLAT) {
-    if (ag_plan_for(a.nranks).unroll == 2) return launch_ag_flat<DT, 2>(a, grid, s);
-    return launch_ag_flat<DT, 1>(a, grid, s);
+  if (kind == KIND_ALLGATHER && a.shape == kShapeAgBase + AG_TILE) {
+    switch (ag_plan_for(a.nranks).unroll) {
+      case 1: return launch_ag_tile<DT, 1>(a, grid, s);
+      case 2: return launch_ag_tile<DT, 2>(a, grid, s);
+      default: return launch_ag_tile<DT, 4>(a, grid, s);
+    }
   }
   if (kind == KIND_RING_AG_STEP) return launch_ring_ag_step<DT>(a, grid, s);
   return launch_programmatic(ag_copy_kernel<DT, AgShape>, grid, AgShape::kThreads, 0, s, a);
