@@ -220,11 +220,7 @@ ra_status_t sm_budget(int max_sms, int* sms) {
 
 // Grid: blockIdx.y = chunk (or rank, for the ring steps); blockIdx.x = CTAs
 // sharing it, enough to cover its vectors but no more than one resident wave
-// of the launch shape on the SM budget (RA_ONE_WAVE, a build-time tunable:
-// 0 lets the fused kernels take one CTA per trip instead).
-#ifndef RA_ONE_WAVE
-#define RA_ONE_WAVE 1
-#endif
+// of the launch shape on the SM budget; a one-trip shape takes a CTA per trip.
 ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3* grid) {
   int threads, per_thread, min_blocks, sms = 0;
   if (shape == ra::kShapeAgBase + ra::AG_TILE) {
@@ -256,14 +252,8 @@ ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3*
   const uint64_t per_cta = a.vec_ok ? (uint64_t)threads * per_thread : (uint64_t)threads;
   uint64_t gx = (work + per_cta - 1) / per_cta;
   const uint64_t cap = (uint64_t)sms * min_blocks / n;
-#if RA_ONE_WAVE
-  if (gx > cap) gx = cap;
-#else  // tuning sweeps: as many CTAs as trips of the shape (each CTA makes one trip)
-  if (shape >= ra::kShapeAgBase || shape == ra::SHAPE_STEP || max_sms > 0) {
-    if (gx > cap) gx = cap;
-  }
+  if (!ra::is_trip_shape(shape) && gx > cap) gx = cap;
   if (gx > 0x7fffffffull) return RA_ERR_UNSUPPORTED;
-#endif
   if (gx < 1) gx = 1;
   *grid = dim3((unsigned)gx, (unsigned)a.nranks);
   return RA_SUCCESS;
@@ -429,6 +419,26 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
   return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
 }
 
+// The one-trip shape for a fused call, or -1 to keep the one-wave shape:
+// all-reduces from N = 3 and reduce-scatters from N = 8, in the buffer dtype
+// (fp32 partials keep their shapes), on every SM (an SM budget caps the grid
+// by definition). RA_GRID_MODE, a build-time tunable for sweeps: -1 this rule,
+// 0 never, 1 wherever a trip shape exists.
+#ifndef RA_GRID_MODE
+#define RA_GRID_MODE -1
+#endif
+int trip_shape_for(int kind, int nranks, bool acc32, bool minmax, int max_sms) {
+  if (acc32 || max_sms > 0 || kind == ra::KIND_ALLGATHER) return -1;
+  const int trip = (kind == ra::KIND_REDUCE_SCATTER && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S;
+#if RA_GRID_MODE >= 0
+  (void)nranks;
+  return RA_GRID_MODE == 1 ? trip : -1;
+#else
+  if (kind == ra::KIND_REDUCE_SCATTER) return nranks >= 8 ? trip : -1;
+  return nranks >= 3 ? trip : -1;
+#endif
+}
+
 ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, size_t count, ra_dtype_t dtype,
                 ra_op_t op, int nranks, void* stream, const ra_options_t* options = &kDefaultOptions) {
   ra::Args a;
@@ -469,9 +479,13 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
                                        : shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
                                                    dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
                                                    op == RA_MIN || op == RA_MAX);
-  if (kind == ra::KIND_REDUCE_SCATTER && a.vec_ok && rs_needs_offgrid(a, recvbufs, elem_size(dtype)))
+  if (kind == ra::KIND_REDUCE_SCATTER && a.vec_ok && rs_needs_offgrid(a, recvbufs, elem_size(dtype))) {
     a.shape = a.acc32 ? ra::SHAPE_RS_OFFGRID_M
                       : (a.shape == ra::SHAPE_S ? ra::SHAPE_RS_OFFGRID : ra::SHAPE_RS_OFFGRID_B2);
+  } else {
+    const int trip = trip_shape_for(kind, nranks, a.acc32 != 0, op == RA_MIN || op == RA_MAX, max_sms);
+    if (trip >= 0) a.shape = trip;
+  }
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
   if (st != RA_SUCCESS) return st;

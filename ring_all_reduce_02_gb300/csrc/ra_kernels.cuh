@@ -142,6 +142,17 @@ using ShapeRS = ShapeS;
 using ShapeMB8 = ShapeS;
 using ShapeW8 = ShapeS;
 #endif
+// Shapes of one-trip launches (a CTA per trip of the chunk; each CTA does one
+// trip and exits). Short-lived CTAs stream HBM faster on GB300 than resident
+// ones that grid-stride, and with one trip per CTA the occupancy the registers
+// allow is what keeps bytes in flight, so these shapes are small. From sweeps
+// of seven shapes (fp32 and bf16, avg and max, 128 MiB and 1 GiB over all
+// ranks, back to back): all-reduce N = 3..16 103-105% of the copy bandwidth at
+// 1 GiB with 128 x 1 at 8 CTAs/SM and loads of 4 ranks (the one-wave shapes:
+// 96-100%), 91-98% at 128 MiB (85-94%); reduce-scatter from N = 8 104-107%
+// (100-104%), min/max on 128 x 2 at 4 CTAs/SM.
+using TripS = Shape<128, 8, 1, 4>;
+using TripRS2 = Shape<128, 4, 2, 4>;
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
 // vector grid at a 2-byte offset, on ShapeS, ShapeRS2 (where the plain call
 // would take loads of 2 ranks at a time) or ShapeM (fp32 partials).
@@ -160,8 +171,14 @@ enum ShapeId {
   SHAPE_RS_OFFGRID_B2 = 11,
   SHAPE_MB8 = 12,
   SHAPE_RS6 = 13,
-  SHAPE_W8 = 14
+  SHAPE_W8 = 14,
+  SHAPE_TRIP_S = 15,    // TripS, one trip per CTA (all-reduce; reduce-scatter sum/avg/prod)
+  SHAPE_TRIP_RS2 = 16   // TripRS2, one trip per CTA (reduce-scatter min/max)
 };
+// A launch that takes a CTA per trip instead of one resident wave.
+__host__ __device__ constexpr bool is_trip_shape(int shape) {
+  return shape == SHAPE_TRIP_S || shape == SHAPE_TRIP_RS2;
+}
 
 enum Kind {
   KIND_ALLREDUCE = 0,       // fused: one launch per call
@@ -191,36 +208,35 @@ struct Args {
 // [begin, end) in steps of stride; in each trip this warp takes the 32
 // vectors base + slot0 + u * uslot + lane (u < kUnroll); vectors at or past
 // `end` are skipped. Trip bases are the same for every thread of the CTA.
+// TRIP: the grid has a CTA per trip of the chunk, and CTA x takes the x-th
+// CTA-sized block of it, whatever the schedule.
 struct Walk {
   uint64_t begin, end, stride;
   uint32_t slot0, uslot;  // offsets inside one trip (less than stride)
 };
-template <class SH>
+template <class SH, bool TRIP>
 __device__ __forceinline__ Walk cta_walk(uint64_t nv) {
   constexpr uint32_t kThreads = SH::kThreads, kUnroll = SH::kUnroll, kWarps = kThreads / 32;
   const uint32_t wid = threadIdx.x / 32;
   Walk w;
-#if RA_SCHEDULE == 1
-  const uint64_t trip = (uint64_t)kThreads * kUnroll;
-  const uint64_t per = ((nv + gridDim.x - 1) / gridDim.x + trip - 1) / trip * trip;
-  w.begin = (uint64_t)blockIdx.x * per;
-  w.end = w.begin + per < nv ? w.begin + per : nv;
-  w.stride = trip;
-  w.slot0 = wid * 32;
-  w.uslot = kThreads;
-#elif RA_SCHEDULE == 2
-  w.begin = 0;
-  w.end = nv;
-  w.stride = (uint64_t)gridDim.x * kThreads * kUnroll;
-  w.slot0 = (wid * gridDim.x + blockIdx.x) * 32;
-  w.uslot = kWarps * gridDim.x * 32;
-#else
   w.begin = 0;
   w.end = nv;
   w.stride = (uint64_t)gridDim.x * kThreads * kUnroll;
   w.slot0 = blockIdx.x * kThreads * kUnroll + wid * 32;
   w.uslot = kThreads;
+  if constexpr (!TRIP) {
+#if RA_SCHEDULE == 1
+    const uint64_t trip = (uint64_t)kThreads * kUnroll;
+    const uint64_t per = ((nv + gridDim.x - 1) / gridDim.x + trip - 1) / trip * trip;
+    w.begin = (uint64_t)blockIdx.x * per;
+    w.end = w.begin + per < nv ? w.begin + per : nv;
+    w.stride = trip;
+    w.slot0 = wid * 32;
+#elif RA_SCHEDULE == 2
+    w.slot0 = (wid * gridDim.x + blockIdx.x) * 32;
+    w.uslot = kWarps * gridDim.x * 32;
 #endif
+  }
   return w;
 }
 
@@ -368,14 +384,14 @@ __device__ __forceinline__ void for_each_edge_elem(uint64_t b0, uint64_t vb, uin
 // ---------------------------------------------------------------------------
 // The all-reduce of the element range [b0, b1), one chunk of one collective,
 // folded in ring order from rank c: whole vectors, then the edge elements.
-template <int DT, int OP, bool ACC32, class SH>
+template <int DT, int OP, bool ACC32, class SH, bool TRIP>
 __device__ __forceinline__ void ar_range(const Args& a, int c, int n, uint64_t b0, uint64_t b1) {
   constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
-  const Walk w = cta_walk<SH>((ve - vb) / V);
+  const Walk w = cta_walk<SH, TRIP>((ve - vb) / V);
   // a thread's first vector of each trip; its later unroll slots lie further on
   for (uint64_t j0 = w.begin + w.slot0 + (threadIdx.x & 31u); j0 < w.end; j0 += w.stride) {
     uint64_t off[kUnroll];
@@ -401,11 +417,13 @@ __device__ __forceinline__ void ar_range(const Args& a, int c, int n, uint64_t b
   });
 }
 
-template <int DT, int OP, bool ACC32, class SH>
+// TRIP: launched with a CTA per trip of the chunk (each CTA does one trip and
+// exits) instead of one resident wave.
+template <int DT, int OP, bool ACC32, class SH, bool TRIP>
 __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_fused_kernel(const __grid_constant__ Args a) {
   pdl_enter();
   const int n = a.nranks, c = blockIdx.y;
-  ar_range<DT, OP, ACC32, SH>(a, c, n, chunk_begin(c, n, a.count), chunk_begin(c + 1, n, a.count));
+  ar_range<DT, OP, ACC32, SH, TRIP>(a, c, n, chunk_begin(c, n, a.count), chunk_begin(c + 1, n, a.count));
 }
 
 // ---------------------------------------------------------------------------
@@ -432,14 +450,14 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ar_group_kernel(
   const int n = a.nranks, c = blockIdx.y;
   for (uint32_t b = 0; b < g.nbuckets; ++b) {
     const uint64_t at = g.begin[b], len = g.count[b];
-    ar_range<DT, OP, ACC32, SH>(a, c, n, at + chunk_begin(c, n, len), at + chunk_begin(c + 1, n, len));
+    ar_range<DT, OP, ACC32, SH, false>(a, c, n, at + chunk_begin(c, n, len), at + chunk_begin(c + 1, n, len));
   }
 }
 
 // ---------------------------------------------------------------------------
 // reduce-scatter: chunk c's fold goes to dst[c], compact (element i -> i - b0)
 // ---------------------------------------------------------------------------
-template <int DT, int OP, bool ACC32, class SH, bool OFFGRID = false>
+template <int DT, int OP, bool ACC32, class SH, bool OFFGRID = false, bool TRIP = false>
 __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(const __grid_constant__ Args a) {
   pdl_enter();
   constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
@@ -449,7 +467,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
-  const Walk w = cta_walk<SH>((ve - vb) / V);
+  const Walk w = cta_walk<SH, TRIP>((ve - vb) / V);
   void* out = a.dst[c];
   const bool out_vec = (a.compact_aligned >> c) & 1u;
   // Off the vector grid the plain kernel stores each lane's vector in 4-byte
@@ -512,7 +530,7 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ag_copy_kernel(c
   const uint64_t b0 = chunk_begin(c, n, a.count), b1 = chunk_begin(c + 1, n, a.count);
   uint64_t vb = b0, ve = b0;
   if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
-  const Walk w = cta_walk<SH>((ve - vb) / V);
+  const Walk w = cta_walk<SH, false>((ve - vb) / V);
   const void* in = a.src[c];
   const bool in_vec = (a.compact_aligned >> c) & 1u;
   for (uint64_t j0 = w.begin + w.slot0 + (threadIdx.x & 31u); j0 < w.end; j0 += w.stride) {
@@ -555,13 +573,13 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) ag_copy_kernel(c
 // ---------------------------------------------------------------------------
 // host-side launch for one dtype (instantiated once per dtype translation unit)
 // ---------------------------------------------------------------------------
-template <int DT, int OP, bool ACC32, class SH>
+template <int DT, int OP, bool ACC32, class SH, bool TRIP = false>
 cudaError_t launch_ar(const Args& a, dim3 grid, cudaStream_t s) {
-  return launch_programmatic(ar_fused_kernel<DT, OP, ACC32, SH>, grid, SH::kThreads, 0, s, a);
+  return launch_programmatic(ar_fused_kernel<DT, OP, ACC32, SH, TRIP>, grid, SH::kThreads, 0, s, a);
 }
-template <int DT, int OP, bool ACC32, class SH, bool OFFGRID = false>
+template <int DT, int OP, bool ACC32, class SH, bool OFFGRID = false, bool TRIP = false>
 cudaError_t launch_rs(const Args& a, dim3 grid, cudaStream_t s) {
-  return launch_programmatic(rs_fused_kernel<DT, OP, ACC32, SH, OFFGRID>, grid, SH::kThreads, 0, s, a);
+  return launch_programmatic(rs_fused_kernel<DT, OP, ACC32, SH, OFFGRID, TRIP>, grid, SH::kThreads, 0, s, a);
 }
 template <int DT, int OP, bool ACC32, class SH>
 cudaError_t launch_fused_shape(int kind, const Args& a, dim3 grid, cudaStream_t s) {
@@ -671,6 +689,17 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
     case SHAPE_W8:
       if (!rs) return launch_ar<DT, OP, ACC32, ShapeW8>(a, grid, s);
       break;
+    case SHAPE_TRIP_S:
+      if constexpr (!ACC32) {
+        if (rs) return launch_rs<DT, OP, false, TripS, false, true>(a, grid, s);
+        return launch_ar<DT, OP, false, TripS, true>(a, grid, s);
+      }
+      break;
+    case SHAPE_TRIP_RS2:
+      if constexpr (!ACC32) {
+        if (rs) return launch_rs<DT, OP, false, TripRS2, false, true>(a, grid, s);
+      }
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -708,6 +737,8 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_RS: return shape_params_of<ShapeRS>(threads, unroll, min_blocks);
     case SHAPE_MB8: return shape_params_of<ShapeMB8>(threads, unroll, min_blocks);
     case SHAPE_W8: return shape_params_of<ShapeW8>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_S: return shape_params_of<TripS>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
     default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
   }
 }
