@@ -11,6 +11,7 @@ fraction of the algorithmic traffic 2*N*S per launch.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
     python bench.py --sweep OUT.jsonl      # message-size sweep, one line per (N, size, call)
     python bench.py --overlap              # bucketed all-reduce beside a synthetic backward pass
+    python bench.py --roofs                # read/write stream rates the kernels are compared against
 """
 
 from __future__ import annotations
@@ -683,6 +684,105 @@ def run_overlap(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# stream roofs (not the headline): what HBM gives to reads and to writes from
+# persistent and from one-shot CTAs, beside torch's copy and fill and the
+# library's all-gather
+# ---------------------------------------------------------------------------
+def run_roofs(args):
+    import ctypes
+
+    import torch
+
+    from ring_all_reduce_02_gb300 import build, ra
+
+    build.build()
+    probe = ctypes.CDLL(build.build_probe())
+    probe.rp_store.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_size_t,
+                               ctypes.c_void_p]
+    probe.rp_load.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    peak, peak_kind = measured_peaks()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(int(2 * l2), dtype=torch.uint8, device="cuda")
+    evict = torch.ones(int(2 * l2) // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    total = 4 << 30
+    big = torch.empty(total, dtype=torch.uint8, device="cuda")
+    other = torch.empty(total // 2, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def check(rc):
+        if rc:
+            raise RuntimeError(f"stream probe failed: cudaError {rc}")
+
+    def store(one_shot, bufs):
+        arr = (ctypes.c_void_p * len(bufs))(*[b.data_ptr() for b in bufs])
+        return lambda: check(probe.rp_store(one_shot, arr, len(bufs), bufs[0].numel(), stream.cuda_stream))
+
+    def load(one_shot, buf):
+        return lambda: check(probe.rp_load(one_shot, buf.data_ptr(), buf.numel(), sink.data_ptr(), stream.cuda_stream))
+
+    def timed(fn, nbytes, label, extra=None):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        clean = []
+        for _ in range(10):  # each launch from an L2 of clean, unrelated lines
+            flush.zero_()
+            torch.amax(evict)
+            torch.cuda._sleep(200_000)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            clean.append(a.elapsed_time(b) * 1e-3)
+        torch.cuda._sleep(200_000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        b2b = a.elapsed_time(b) * 1e-3 / reps
+        rec = {"mode": "roofs", "what": label, "bytes": nbytes,
+               "clean_GBps": round(nbytes / statistics.median(clean) / GB, 1),
+               "b2b_GBps": round(nbytes / b2b / GB, 1),
+               "b2b_frac_of_copy_peak": round(nbytes / b2b / GB / peak, 4), "peak": f"{peak} ({peak_kind})"}
+        rec.update(extra or {})
+        print(json.dumps(rec), flush=True)
+
+    sampler = ClockSampler(dev).start()
+    time.sleep(0.3)
+    t0 = time.time()
+    f32 = big.view(torch.float32)
+    timed(lambda: other.view(torch.float32).copy_(f32[: total // 8]), total, "torch copy_ (read 2 GiB + write 2 GiB)")
+    timed(lambda: f32.fill_(1.5), total, "torch fill_ (write 4 GiB)")
+    timed(store(0, [big]), total, "store stream, persistent CTAs (write 4 GiB)")
+    timed(store(1, [big]), total, "store stream, one-shot CTAs (write 4 GiB)")
+    timed(load(0, big), total, "load stream, persistent CTAs (read 4 GiB)")
+    timed(load(1, big), total, "load stream, one-shot CTAs (read 4 GiB)")
+    for n in (8, 16):
+        bufs = [big[r * (total // n):(r + 1) * (total // n)] for r in range(n)]
+        timed(store(0, bufs), total, f"store stream to {n} buffers, persistent CTAs (write 4 GiB)")
+        timed(store(1, bufs), total, f"store stream to {n} buffers, one-shot CTAs (write 4 GiB)")
+        length = (1 << 30) // 4 // n
+        bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+        shards = [torch.randn(e - b, device="cuda") for b, e in bounds]
+        recvs = [torch.empty(length, device="cuda") for _ in range(n)]
+        timed(lambda: ra.ra_allgather(shards, recvs, stream=stream), (n + 1) * length * 4,
+              f"library all-gather, N = {n}, fp32, 1 GiB over all ranks", {"nranks": n})
+        del shards, recvs
+    t1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    print(json.dumps({"mode": "roofs", "clocks": sampler.summary(t0, t1)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -697,6 +797,8 @@ def main():
     ap.add_argument("--overlap-tokens", type=int, default=2048)
     ap.add_argument("--call", default=None, choices=sorted(CALLS),
                     help="time one call alone on the workload (per-kernel roofline; not the headline)")
+    ap.add_argument("--roofs", action="store_true",
+                    help="stream roofs: reads and writes from persistent and one-shot CTAs (not the headline)")
     ap.add_argument("--case", default=None, metavar="N,COUNT,DTYPE,OP",
                     help="with --call: this case instead of the named workload (e.g. 16,16777216,f32,sum)")
     args = ap.parse_args()
@@ -708,6 +810,8 @@ def main():
         return run_sweep(args)
     if args.overlap:
         return run_overlap(args)
+    if args.roofs:
+        return run_roofs(args)
     if args.call:
         return run_call(args)
     return run_ours(args)

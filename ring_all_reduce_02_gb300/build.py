@@ -96,5 +96,24 @@ def build(force: bool = False, verbose: bool = False, defines=(), lib_path: str 
     return lib_path
 
 
+PROBE_SRC = os.path.join(HERE, "probe", "stream_probe.cu")
+PROBE_LIB = os.path.join(HERE, "libra_probe.so")
+
+
+def build_probe(force: bool = False) -> str:
+    """Compile the stream probes (measurement kernels, not the collective path) into libra_probe.so."""
+    if not force and os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) >= os.path.getmtime(PROBE_SRC):
+        return PROBE_LIB
+    tmp = PROBE_LIB + ".tmp"
+    cmd = [_nvcc(), *ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-cudart", "static",
+           PROBE_SRC, "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on stream_probe.cu:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
+
+
 if __name__ == "__main__":
     print(build(force=True, verbose="--verbose" in sys.argv))
+    print(build_probe(force=True))
