@@ -626,7 +626,7 @@ def run_overlap(args):
         for b, x in enumerate(xs):
             torch.matmul(x, gy, out=outs[b])
             if events is not None:
-                events[b].record(cs)
+                events[b].record(torch.cuda.current_stream())
 
     def timed(fn, reps=5):
         for _ in range(2):
@@ -664,6 +664,17 @@ def run_overlap(args):
         main.wait_stream(cs)
         main.wait_stream(ms)
 
+    def overlapped_on(cs_, ms_, engine="registers"):
+        events = [torch.cuda.Event() for _ in plan]
+        cs_.wait_stream(main)
+        ms_.wait_stream(main)
+        with torch.cuda.stream(cs_):
+            compute(events)
+        ra.ra_allreduce_buckets(sends, recvs, plan, op, ready_events=events, engine=engine, status=status,
+                                stream=ms_)
+        main.wait_stream(cs_)
+        main.wait_stream(ms_)
+
     c_ms = timed(compute_only)
     flops = sum(2 * c * tokens for _, c in plan)
     s_bytes = length * 2
@@ -681,7 +692,76 @@ def run_overlap(args):
                "overlapped_ms": round(t_ms, 3), "exposed_comm_ms": round(t_ms - c_ms, 3),
                "hidden_fraction": round((c_ms + a_ms - t_ms) / a_ms, 3), "status": int(status.item())}
         print(json.dumps(rec), flush=True)
+
+    # SM partitions: the GEMMs on one green context, the all-reduces on another with k SMs
+    a_all = timed(lambda: comm_only(0, "registers", ms_normal))
+    for k in (16, 32, 48, 64, 96):
+        try:
+            (ms_k, k_sms), (cs_k, rest_sms) = green_partition(k)
+        except RuntimeError as e:  # no green contexts here: say so and stop the sweep
+            print(json.dumps({"mode": "overlap_split", "unavailable": str(e)}), flush=True)
+            break
+        for engine in ("registers", "bulk"):
+            def comm_k():
+                ms_k.wait_stream(main)
+                ra.ra_allreduce_buckets(sends, recvs, plan, op, engine=engine, status=status, stream=ms_k)
+                main.wait_stream(ms_k)
+
+            def compute_k():
+                cs_k.wait_stream(main)
+                with torch.cuda.stream(cs_k):
+                    compute()
+                main.wait_stream(cs_k)
+
+            a_k = timed(comm_k)
+            c_k = timed(compute_k)
+            t_k = timed(lambda: overlapped_on(cs_k, ms_k, engine))
+            rec = {"mode": "overlap_split", "workload": "ar_n8_bf16_avg_gpt2m", "buckets": len(plan), "tokens": tokens,
+                   "engine": engine, "comm_sms": k_sms, "compute_sms": rest_sms,
+                   "allreduce_ms_on_comm_sms": round(a_k, 3),
+                   "allreduce_hbm_GBps_per_comm_sm": round(2 * n * s_bytes / (a_k * 1e-3) / GB / k_sms, 1),
+                   "compute_ms_on_compute_sms": round(c_k, 3), "overlapped_ms": round(t_k, 3),
+                   "unsplit_compute_ms": round(c_ms, 3), "unsplit_allreduce_ms": round(a_all, 3),
+                   "hidden_fraction": round((c_ms + a_all - t_k) / a_all, 3), "status": int(status.item())}
+            print(json.dumps(rec), flush=True)
     return 0
+
+
+_green = {}
+
+
+def green_partition(k):
+    """Two CUDA green contexts on device 0: one with k SMs, one with the rest; a stream on each.
+    Returns ((stream_k, sms_k), (stream_rest, sms_rest)). Driver API through ctypes."""
+    import ctypes
+
+    import torch
+
+    if k in _green:
+        return _green[k]
+    cu = ctypes.CDLL("libcuda.so.1")
+
+    def ck(res, what):
+        if res != 0:
+            raise RuntimeError(f"{what} failed (CUresult {res})")
+
+    dev = ctypes.c_int()
+    ck(cu.cuDeviceGet(ctypes.byref(dev), 0), "cuDeviceGet")
+    Res = ctypes.c_ubyte * 144  # CUdevResource: type, 92 bytes of padding, then the SM counts
+    whole, part, rest = Res(), Res(), Res()
+    ck(cu.cuDeviceGetDevResource(dev, ctypes.byref(whole), 1), "cuDeviceGetDevResource")
+    nb = ctypes.c_uint(1)
+    ck(cu.cuDevSmResourceSplitByCount(ctypes.byref(part), ctypes.byref(nb), ctypes.byref(whole), ctypes.byref(rest),
+                                      0, k), "cuDevSmResourceSplitByCount")
+    out = []
+    for r in (part, rest):
+        desc, ctx, stream = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+        ck(cu.cuDevResourceGenerateDesc(ctypes.byref(desc), ctypes.byref(r), 1), "cuDevResourceGenerateDesc")
+        ck(cu.cuGreenCtxCreate(ctypes.byref(ctx), desc, dev, 1), "cuGreenCtxCreate")
+        ck(cu.cuGreenCtxStreamCreate(ctypes.byref(stream), ctx, 1, 0), "cuGreenCtxStreamCreate")
+        out.append((torch.cuda.ExternalStream(stream.value), int.from_bytes(bytes(r[96:100]), "little")))
+    _green[k] = tuple(out)
+    return _green[k]
 
 
 # ---------------------------------------------------------------------------
