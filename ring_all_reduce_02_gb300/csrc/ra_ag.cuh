@@ -27,11 +27,6 @@ namespace ra {
 constexpr int kAgThreads = 256;
 using AgShape = Shape<kAgThreads, 2, 1, 1>;  // the register kernel
 
-#ifndef RA_AG_STAGES
-#define RA_AG_STAGES 2
-#endif
-constexpr uint32_t kAgStages = RA_AG_STAGES;  // tiles in shared memory per CTA
-
 enum AgKernel { AG_REGISTERS = 0, AG_TILE = 1 };
 constexpr int kShapeAgBase = 100;  // Args::shape of an all-gather launch: kShapeAgBase + AgKernel
 
