@@ -197,8 +197,12 @@ ra_status_t ra_bucket_plan(const size_t* param_counts, int nparams, size_t bucke
  * ready_events[b] (a cudaEvent_t the producer recorded when the bucket's
  * gradients were complete; NULL entries or a NULL array wait for nothing).
  * The waits and launches are enqueued on `stream` in bucket order, so buckets
- * overlap with work on other streams as soon as they are ready. Buffers,
- * in-place rule and options as ra_allreduce_ex.
+ * overlap with work on other streams as soon as they are ready. A run of
+ * buckets with no ready event of their own (NULL entries, or a NULL array)
+ * goes out as one grouped launch of up to 64 buckets when the options are the
+ * default engine and ring order; each bucket's result bits are still those of
+ * an all-reduce of its own. Buffers, in-place rule and options as
+ * ra_allreduce_ex.
  */
 ra_status_t ra_allreduce_buckets(const void* const* sendbufs, void* const* recvbufs, size_t count,
                                  ra_dtype_t dtype, ra_op_t op, int nranks, int nbuckets, const size_t* bucket_begin,

@@ -221,7 +221,7 @@ ra_status_t sm_budget(int max_sms, int* sms) {
 // Grid: blockIdx.y = chunk (or rank, for the ring steps); blockIdx.x = CTAs
 // sharing it, enough to cover its vectors but no more than one resident wave
 // of the launch shape on the SM budget; a one-trip shape takes a CTA per trip.
-ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3* grid) {
+ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3* grid, bool step_trip = false) {
   int threads, per_thread, min_blocks, sms = 0;
   if (shape == ra::kShapeAgBase + ra::AG_TILE) {
     // one CTA per whole tile of the longest chunk, plus one per chunk for its leftovers
@@ -252,7 +252,8 @@ ra_status_t grid_for(const ra::Args& a, int dtype, int shape, int max_sms, dim3*
   const uint64_t per_cta = a.vec_ok ? (uint64_t)threads * per_thread : (uint64_t)threads;
   uint64_t gx = (work + per_cta - 1) / per_cta;
   const uint64_t cap = (uint64_t)sms * min_blocks / n;
-  if (!ra::is_trip_shape(shape) && gx > cap) gx = cap;
+  const bool one_trip = ra::is_trip_shape(shape) || (shape == ra::SHAPE_STEP && step_trip && max_sms == 0);
+  if (!one_trip && gx > cap) gx = cap;
   if (gx > 0x7fffffffull) return RA_ERR_UNSUPPORTED;
   if (gx < 1) gx = 1;
   *grid = dim3((unsigned)gx, (unsigned)a.nranks);
@@ -426,16 +427,17 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 }
 
 // The one-trip shape for a fused call, or -1 to keep the one-wave shape:
-// all-reduces from N = 3 and reduce-scatters from N = 8, in the buffer dtype
-// (fp32 partials keep their shapes), on every SM (an SM budget caps the grid
-// by definition). RA_GRID_MODE, a build-time tunable for sweeps: -1 this rule,
+// all-reduces from N = 3 and reduce-scatters from N = 8 (with fp32 partials
+// too), on every SM (an SM budget caps the grid by definition). RA_GRID_MODE, a build-time tunable for sweeps: -1 this rule,
 // 0 never, 1 wherever a trip shape exists.
 #ifndef RA_GRID_MODE
 #define RA_GRID_MODE -1
 #endif
 int trip_shape_for(int kind, int nranks, bool acc32, bool minmax, int max_sms) {
-  if (acc32 || max_sms > 0 || kind == ra::KIND_ALLGATHER) return -1;
-  const int trip = (kind == ra::KIND_REDUCE_SCATTER && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S;
+  if (max_sms > 0 || kind == ra::KIND_ALLGATHER) return -1;
+  const bool rs = kind == ra::KIND_REDUCE_SCATTER;
+  const int trip = acc32 ? (rs ? ra::SHAPE_TRIP_ACC_RS2 : ra::SHAPE_TRIP_ACC)
+                         : ((rs && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S);
 #if RA_GRID_MODE >= 0
   (void)nranks;
   return RA_GRID_MODE == 1 ? trip : -1;
@@ -511,7 +513,12 @@ ra_status_t run_ringsteps(const void* const* sendbufs, void* const* recvbufs, si
     st = grid_for(a, dtype, a.shape, 0, &grid);
     return st != RA_SUCCESS ? st : launch(ra::KIND_ALLREDUCE, dtype, op, a, grid, stream);
   }
-  st = grid_for(a, dtype, ra::SHAPE_STEP, 0, &grid);
+  // A CTA per trip from 64 MiB per rank: 8 x 256 MiB fp32 avg 1.336 ms (103.6% of the copy
+  // bandwidth for the schedule's own bytes) against 1.465 ms (94.5%) as one resident wave,
+  // 4 x 256 MiB 101.6 against 94.1%, 16 x 64 MiB 89.9 against 85.4%; at 8 x 32 MiB bf16 it lost
+  // (78.6 against 87.9%).
+  const bool step_trip = (uint64_t)count * (uint64_t)elem_size(dtype) >= (64ull << 20);
+  st = grid_for(a, dtype, ra::SHAPE_STEP, 0, &grid, step_trip);
   if (st != RA_SUCCESS) return st;
   for (int k = 0; k < nsteps; ++k) {
     const bool rs = k < nranks - 1;

@@ -151,6 +151,9 @@ using ShapeW8 = ShapeS;
 // 1 GiB with 128 x 1 at 8 CTAs/SM and loads of 4 ranks (the one-wave shapes:
 // 96-100%), 91-98% at 128 MiB (85-94%); reduce-scatter from N = 8 104-107%
 // (100-104%), min/max on 128 x 2 at 4 CTAs/SM.
+// fp32 partials take TripS for the all-reduce (bf16 avg: 102.5-104.8% at 1 GiB,
+// N = 3..16, against 95.9-99.5% one-wave) and TripRS2 for the reduce-scatter
+// (101.9 / 103.3% at N = 8 / 16 against 96.1 / 98.4%; TripS would spill there).
 using TripS = Shape<128, 8, 1, 4>;
 using TripRS2 = Shape<128, 4, 2, 4>;
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
@@ -173,11 +176,13 @@ enum ShapeId {
   SHAPE_RS6 = 13,
   SHAPE_W8 = 14,
   SHAPE_TRIP_S = 15,    // TripS, one trip per CTA (all-reduce; reduce-scatter sum/avg/prod)
-  SHAPE_TRIP_RS2 = 16   // TripRS2, one trip per CTA (reduce-scatter min/max)
+  SHAPE_TRIP_RS2 = 16,  // TripRS2, one trip per CTA (reduce-scatter min/max)
+  SHAPE_TRIP_ACC = 17,  // TripS, one trip per CTA, fp32 partials (all-reduce)
+  SHAPE_TRIP_ACC_RS2 = 18  // TripRS2, one trip per CTA, fp32 partials (reduce-scatter)
 };
 // A launch that takes a CTA per trip instead of one resident wave.
 __host__ __device__ constexpr bool is_trip_shape(int shape) {
-  return shape == SHAPE_TRIP_S || shape == SHAPE_TRIP_RS2;
+  return shape == SHAPE_TRIP_S || shape == SHAPE_TRIP_RS2 || shape == SHAPE_TRIP_ACC || shape == SHAPE_TRIP_ACC_RS2;
 }
 
 enum Kind {
@@ -700,6 +705,16 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (rs) return launch_rs<DT, OP, false, TripRS2, false, true>(a, grid, s);
       }
       break;
+    case SHAPE_TRIP_ACC:
+      if constexpr (ACC32) {
+        if (!rs) return launch_ar<DT, OP, true, TripS, true>(a, grid, s);
+      }
+      break;
+    case SHAPE_TRIP_ACC_RS2:
+      if constexpr (ACC32) {
+        if (rs) return launch_rs<DT, OP, true, TripRS2, false, true>(a, grid, s);
+      }
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -739,6 +754,8 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_W8: return shape_params_of<ShapeW8>(threads, unroll, min_blocks);
     case SHAPE_TRIP_S: return shape_params_of<TripS>(threads, unroll, min_blocks);
     case SHAPE_TRIP_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_ACC: return shape_params_of<TripS>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_ACC_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
     default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
   }
 }
