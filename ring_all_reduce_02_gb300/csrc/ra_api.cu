@@ -427,22 +427,27 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 }
 
 // The one-trip shape for a fused call, or -1 to keep the one-wave shape:
-// all-reduces from N = 3 and reduce-scatters from N = 8 (with fp32 partials
-// too), on every SM (an SM budget caps the grid by definition). RA_GRID_MODE, a build-time tunable for sweeps: -1 this rule,
-// 0 never, 1 wherever a trip shape exists.
+// all-reduces from N = 3, reduce-scatters from N = 8 and, for 4-byte types,
+// from N = 4 (fp32 avg, 1 GiB over all ranks: 105-107% against 101-105%; bf16
+// lost 3-4 points there), fp32 partials and shards off the vector grid
+// included, on every SM (an SM budget caps the grid by definition).
+// RA_GRID_MODE, a build-time tunable for sweeps: -1 this rule, 0 never, 1
+// wherever a trip shape exists.
 #ifndef RA_GRID_MODE
 #define RA_GRID_MODE -1
 #endif
-int trip_shape_for(int kind, int nranks, bool acc32, bool minmax, int max_sms) {
+int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax, bool offgrid, int max_sms) {
   if (max_sms > 0 || kind == ra::KIND_ALLGATHER) return -1;
   const bool rs = kind == ra::KIND_REDUCE_SCATTER;
-  const int trip = acc32 ? (rs ? ra::SHAPE_TRIP_ACC_RS2 : ra::SHAPE_TRIP_ACC)
-                         : ((rs && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S);
+  int trip;
+  if (rs && offgrid) trip = acc32 ? ra::SHAPE_TRIP_RS_OFFGRID_ACC : ra::SHAPE_TRIP_RS_OFFGRID;
+  else if (acc32) trip = rs ? ra::SHAPE_TRIP_ACC_RS2 : ra::SHAPE_TRIP_ACC;
+  else trip = (rs && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S;
 #if RA_GRID_MODE >= 0
-  (void)nranks;
+  (void)nranks, (void)elem_bytes;
   return RA_GRID_MODE == 1 ? trip : -1;
 #else
-  if (kind == ra::KIND_REDUCE_SCATTER) return nranks >= 8 ? trip : -1;
+  if (rs) return (nranks >= 8 || (elem_bytes == 4 && nranks >= 4)) ? trip : -1;
   return nranks >= 3 ? trip : -1;
 #endif
 }
@@ -487,13 +492,14 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
                                        : shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
                                                    dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
                                                    op == RA_MIN || op == RA_MAX);
-  if (kind == ra::KIND_REDUCE_SCATTER && a.vec_ok && rs_needs_offgrid(a, recvbufs, elem_size(dtype))) {
+  const bool offgrid =
+      kind == ra::KIND_REDUCE_SCATTER && a.vec_ok && rs_needs_offgrid(a, recvbufs, elem_size(dtype));
+  if (offgrid)
     a.shape = a.acc32 ? ra::SHAPE_RS_OFFGRID_M
                       : (a.shape == ra::SHAPE_S ? ra::SHAPE_RS_OFFGRID : ra::SHAPE_RS_OFFGRID_B2);
-  } else {
-    const int trip = trip_shape_for(kind, nranks, a.acc32 != 0, op == RA_MIN || op == RA_MAX, max_sms);
-    if (trip >= 0) a.shape = trip;
-  }
+  const int trip =
+      trip_shape_for(kind, nranks, elem_size(dtype), a.acc32 != 0, op == RA_MIN || op == RA_MAX, offgrid, max_sms);
+  if (trip >= 0) a.shape = trip;
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
   if (st != RA_SUCCESS) return st;

@@ -156,6 +156,7 @@ using ShapeW8 = ShapeS;
 // (101.9 / 103.3% at N = 8 / 16 against 96.1 / 98.4%; TripS would spill there).
 using TripS = Shape<128, 8, 1, 4>;
 using TripRS2 = Shape<128, 4, 2, 4>;
+using TripRS1 = Shape<128, 4, 1, 4>;  // reduce-scatter with fp32 partials and 2-byte-offset shards
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
 // vector grid at a 2-byte offset, on ShapeS, ShapeRS2 (where the plain call
 // would take loads of 2 ranks at a time) or ShapeM (fp32 partials).
@@ -178,11 +179,14 @@ enum ShapeId {
   SHAPE_TRIP_S = 15,    // TripS, one trip per CTA (all-reduce; reduce-scatter sum/avg/prod)
   SHAPE_TRIP_RS2 = 16,  // TripRS2, one trip per CTA (reduce-scatter min/max)
   SHAPE_TRIP_ACC = 17,  // TripS, one trip per CTA, fp32 partials (all-reduce)
-  SHAPE_TRIP_ACC_RS2 = 18  // TripRS2, one trip per CTA, fp32 partials (reduce-scatter)
+  SHAPE_TRIP_ACC_RS2 = 18,  // TripRS2, one trip per CTA, fp32 partials (reduce-scatter)
+  SHAPE_TRIP_RS_OFFGRID = 19,  // TripS, one trip per CTA, reduce-scatter with 2-byte-offset shards
+  SHAPE_TRIP_RS_OFFGRID_ACC = 20  // TripRS1, one trip per CTA, the same with fp32 partials
 };
 // A launch that takes a CTA per trip instead of one resident wave.
 __host__ __device__ constexpr bool is_trip_shape(int shape) {
-  return shape == SHAPE_TRIP_S || shape == SHAPE_TRIP_RS2 || shape == SHAPE_TRIP_ACC || shape == SHAPE_TRIP_ACC_RS2;
+  return shape == SHAPE_TRIP_S || shape == SHAPE_TRIP_RS2 || shape == SHAPE_TRIP_ACC || shape == SHAPE_TRIP_ACC_RS2 ||
+         shape == SHAPE_TRIP_RS_OFFGRID || shape == SHAPE_TRIP_RS_OFFGRID_ACC;
 }
 
 enum Kind {
@@ -477,11 +481,14 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
   const bool out_vec = (a.compact_aligned >> c) & 1u;
   // Off the vector grid the plain kernel stores each lane's vector in 4-byte
   // units. OFFGRID (chosen when some chunk's output is only 2-byte aligned
-  // against the grid) sends such a chunk's results out through this slice
-  // instead: a warp's 32 consecutive results, consecutive lanes on consecutive
-  // 2-byte units, so each warp store covers 64 contiguous bytes.
-  __shared__ Vec stage[OFFGRID ? kThreads : 1];
-  const uint32_t lane = threadIdx.x & 31u, wfirst = threadIdx.x & ~31u;
+  // against the grid) realigns such a chunk's results in registers instead:
+  // the warp's 32 consecutive results are one run of bytes that starts 2 bytes
+  // past a 4-byte boundary, so the 4-byte word that starts in lane l's 32
+  // bytes takes its upper half from the lane's next word, and the word that
+  // starts in its first 2 bytes takes its lower half from lane l-1's last word
+  // (a shuffle). Each lane then writes 8 aligned 4-byte words; only the run's
+  // first and last 2 bytes take 2-byte stores.
+  const uint32_t lane = threadIdx.x & 31u;
   // trips are warp-uniform (the warp synchronises on the off-grid path)
   for (uint64_t base = w.begin; base < w.end; base += w.stride) {
     uint64_t off[kUnroll];
@@ -503,14 +510,20 @@ __global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks) rs_fused_kernel(
         char* wdst = static_cast<char*>(out) + (vb + jw * V - b0) * ES;
         if ((reinterpret_cast<uintptr_t>(wdst) & 3u) == 0) {  // the chunk allows 4-byte units
           if (ok[u]) st_vec_units(static_cast<char*>(out) + off[u] - b0 * ES, acc[u]);
-        } else {  // 2-byte units: the warp's results go out through shared memory, lanes on consecutive units
-          const uint32_t bytes = (jw >= w.end ? 0u : (w.end - jw < 32 ? (uint32_t)(w.end - jw) : 32u)) * kVecBytes;
-          stage[threadIdx.x] = acc[u];
-          __syncwarp();
-          const char* sw = reinterpret_cast<const char*>(stage + wfirst);
-          for (uint32_t o = lane * 2u; o < bytes; o += 64u)
-            __stcs(reinterpret_cast<unsigned short*>(wdst + o), *reinterpret_cast<const unsigned short*>(sw + o));
-          __syncwarp();
+        } else {  // 2-byte offset: realign in registers (the branch is warp-uniform: jw is)
+          const uint32_t nvalid = jw >= w.end ? 0u : (w.end - jw < 32 ? (uint32_t)(w.end - jw) : 32u);
+          const Vec& v = acc[u];
+          const uint32_t prev = __shfl_up_sync(0xffffffffu, v.w[kVecWords - 1], 1);
+          if (lane < nvalid) {
+            char* mine = wdst + lane * kVecBytes;  // this lane's 32 bytes start here, 2 bytes past a word
+            unsigned int* q = reinterpret_cast<unsigned int*>(mine - 2);
+            if (lane == 0) __stcs(reinterpret_cast<unsigned short*>(mine), (unsigned short)(v.w[0] & 0xffffu));
+            else __stcs(q, (prev >> 16) | (v.w[0] << 16));
+#pragma unroll
+            for (int k = 1; k < kVecWords; ++k) __stcs(q + k, (v.w[k - 1] >> 16) | (v.w[k] << 16));
+            if (lane == nvalid - 1)
+              __stcs(reinterpret_cast<unsigned short*>(mine + kVecBytes - 2), (unsigned short)(v.w[kVecWords - 1] >> 16));
+          }
         }
       } else if (ok[u]) {
         st_vec_units(static_cast<char*>(out) + off[u] - b0 * ES, acc[u]);
@@ -715,6 +728,16 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (rs) return launch_rs<DT, OP, true, TripRS2, false, true>(a, grid, s);
       }
       break;
+    case SHAPE_TRIP_RS_OFFGRID:
+      if constexpr (!ACC32 && Elem<DT>::kSize == 2) {
+        if (rs) return launch_rs<DT, OP, false, TripS, true, true>(a, grid, s);
+      }
+      break;
+    case SHAPE_TRIP_RS_OFFGRID_ACC:
+      if constexpr (ACC32) {
+        if (rs) return launch_rs<DT, OP, true, TripRS1, true, true>(a, grid, s);
+      }
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -756,6 +779,8 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_TRIP_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
     case SHAPE_TRIP_ACC: return shape_params_of<TripS>(threads, unroll, min_blocks);
     case SHAPE_TRIP_ACC_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_RS_OFFGRID: return shape_params_of<TripS>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_RS_OFFGRID_ACC: return shape_params_of<TripRS1>(threads, unroll, min_blocks);
     default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
   }
 }

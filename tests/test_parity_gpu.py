@@ -325,11 +325,12 @@ def test_offset_views(ra, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("n", [3, 4, 6])
+@pytest.mark.parametrize("n", [3, 4, 6, 8, 12])
 def test_offgrid_compact_buffers_many_tiles(ra, dtype, n):
     # compact RS outputs / AG inputs at every phase against the vector grid, with chunks several
     # all-gather tiles (256 vectors) long: the unit-wise tile loads of the all-gather, the 4-byte
-    # per-lane and 2-byte cooperative reduce-scatter stores
+    # per-lane and 2-byte cooperative reduce-scatter stores (one resident wave below N = 8 for
+    # 2-byte types, a CTA per trip from there)
     es = ELEM_SIZE[dtype]
     per_vec = ra.ra_vector_bytes() // es
     length = n * 256 * per_vec * 3 + 13
@@ -350,6 +351,28 @@ def test_offgrid_compact_buffers_many_tiles(ra, dtype, n):
             assert outs[c].canaries_intact() and recvs[c].canaries_intact(), f"off {off} chunk {c}"
             assert_same_bits(to_host(outs[c].view, dtype), shards_want[c], dtype, f"RS off {off} chunk {c}")
             assert_same_bits(to_host(recvs[c].view, dtype), want[c], dtype, f"AG off {off} rank {c}")
+
+
+@pytest.mark.parametrize("n", [3, 8, 12])
+def test_offgrid_shards_fp32_partials(ra, n):
+    # reduce-scatter with fp32 partials into bf16 shards at every 2-byte phase against the vector
+    # grid (the cooperative off-grid stores; one wave at N = 3, a CTA per trip from N = 8)
+    dtype = "bf16"
+    per_vec = ra.ra_vector_bytes() // ELEM_SIZE[dtype]
+    length = n * 128 * per_vec * 3 + 13
+    xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=90 + n)
+    want, _ = oracle.allreduce_ex(xs, "avg", dtype, accum="fp32")
+    bounds = [oracle.chunk_range(length, n, c) for c in range(n)]
+    for off in (0, 1, 2, 3, per_vec - 1):
+        sends = [Padded(length, dtype) for _ in range(n)]
+        for b, x in zip(sends, xs):
+            b.fill(x)
+        outs = [Padded(e - b, dtype, off + c) for c, (b, e) in enumerate(bounds)]
+        ra.ra_reduce_scatter_ex([b.view for b in sends], [o.view for o in outs], "avg", accum="fp32")
+        torch.cuda.synchronize()
+        for c, (b, e) in enumerate(bounds):
+            assert outs[c].canaries_intact(), f"off {off} chunk {c}"
+            assert_same_bits(to_host(outs[c].view, dtype), want[0][b:e], dtype, f"off {off} chunk {c}")
 
 
 def test_fewer_elements_than_ranks(ra):
