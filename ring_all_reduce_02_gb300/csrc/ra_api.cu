@@ -78,7 +78,9 @@ bool overlaps(const Range& a, const Range& b) {
 int shape_for(int nranks, bool reduce_scatter = false, bool acc32 = false, bool narrow = false,
               bool minmax = false) {
   if (reduce_scatter) {
-    if (acc32) return ra::SHAPE_M;
+    // fp32 partials: 128 x 1 at 8 CTAs/SM with loads of 2 ranks (bf16 avg, 1 GiB over all
+    // ranks, N = 3..7: 96.5-99.5% of the copy bandwidth against 72-90% on ShapeM)
+    if (acc32) return ra::SHAPE_RS2;
     if (nranks <= 3) return (narrow && !minmax) ? ra::SHAPE_RS2 : ra::SHAPE_RS6;
     return minmax ? ra::SHAPE_RS : ra::SHAPE_S;
   }
@@ -430,7 +432,8 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 // all-reduces from N = 3, reduce-scatters from N = 8 and, for 4-byte types,
 // from N = 4 (fp32 avg, 1 GiB over all ranks: 105-107% against 101-105%; bf16
 // lost 3-4 points there), fp32 partials and shards off the vector grid
-// included, on every SM (an SM budget caps the grid by definition).
+// included, but not both at once (bf16 avg at N = 12, 1 GiB: 96.7% one-wave
+// against 90.0%), on every SM (an SM budget caps the grid by definition).
 // RA_GRID_MODE, a build-time tunable for sweeps: -1 this rule, 0 never, 1
 // wherever a trip shape exists.
 #ifndef RA_GRID_MODE
@@ -439,8 +442,9 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax, bool offgrid, int max_sms) {
   if (max_sms > 0 || kind == ra::KIND_ALLGATHER) return -1;
   const bool rs = kind == ra::KIND_REDUCE_SCATTER;
+  if (rs && offgrid && acc32) return -1;
   int trip;
-  if (rs && offgrid) trip = acc32 ? ra::SHAPE_TRIP_RS_OFFGRID_ACC : ra::SHAPE_TRIP_RS_OFFGRID;
+  if (rs && offgrid) trip = ra::SHAPE_TRIP_RS_OFFGRID;
   else if (acc32) trip = rs ? ra::SHAPE_TRIP_ACC_RS2 : ra::SHAPE_TRIP_ACC;
   else trip = (rs && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S;
 #if RA_GRID_MODE >= 0

@@ -120,7 +120,7 @@ struct Shape {
 using ShapeS = Shape<128, 8, 1, 4>;   // sum/avg/prod reduce-scatter nranks >= 4; fp16/bf16 sum/avg/prod
                                       // all-reduce and fp32 partials at nranks 1..2
 using ShapeS4 = Shape<128, 4, 2, 2>;  // other all-reduces at nranks 1..2
-using ShapeRS2 = Shape<128, 8, 1, 2>; // fp16/bf16 sum/avg/prod reduce-scatter nranks 1..3
+using ShapeRS2 = Shape<128, 8, 1, 2>; // fp16/bf16 sum/avg/prod reduce-scatter nranks 1..3; fp32 partials below 8
 using ShapeRS6 = Shape<128, 6, 1, 2>; // other reduce-scatters at nranks 1..3
 using ShapeRS = Shape<128, 8, 2, 2>;  // min/max reduce-scatter nranks >= 4
 using ShapeN3 = Shape<256, 1, 4, 4>;  // all-reduce nranks 3
@@ -156,10 +156,9 @@ using ShapeW8 = ShapeS;
 // (101.9 / 103.3% at N = 8 / 16 against 96.1 / 98.4%; TripS would spill there).
 using TripS = Shape<128, 8, 1, 4>;
 using TripRS2 = Shape<128, 4, 2, 4>;
-using TripRS1 = Shape<128, 4, 1, 4>;  // reduce-scatter with fp32 partials and 2-byte-offset shards
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
-// vector grid at a 2-byte offset, on ShapeS, ShapeRS2 (where the plain call
-// would take loads of 2 ranks at a time) or ShapeM (fp32 partials).
+// vector grid at a 2-byte offset, on ShapeS, or on ShapeRS2 (where the plain
+// call would take loads of 2 ranks at a time; _M: with fp32 partials).
 enum ShapeId {
   SHAPE_S = 0,
   SHAPE_N3 = 1,
@@ -180,13 +179,12 @@ enum ShapeId {
   SHAPE_TRIP_RS2 = 16,  // TripRS2, one trip per CTA (reduce-scatter min/max)
   SHAPE_TRIP_ACC = 17,  // TripS, one trip per CTA, fp32 partials (all-reduce)
   SHAPE_TRIP_ACC_RS2 = 18,  // TripRS2, one trip per CTA, fp32 partials (reduce-scatter)
-  SHAPE_TRIP_RS_OFFGRID = 19,  // TripS, one trip per CTA, reduce-scatter with 2-byte-offset shards
-  SHAPE_TRIP_RS_OFFGRID_ACC = 20  // TripRS1, one trip per CTA, the same with fp32 partials
+  SHAPE_TRIP_RS_OFFGRID = 19  // TripS, one trip per CTA, reduce-scatter with 2-byte-offset shards
 };
 // A launch that takes a CTA per trip instead of one resident wave.
 __host__ __device__ constexpr bool is_trip_shape(int shape) {
   return shape == SHAPE_TRIP_S || shape == SHAPE_TRIP_RS2 || shape == SHAPE_TRIP_ACC || shape == SHAPE_TRIP_ACC_RS2 ||
-         shape == SHAPE_TRIP_RS_OFFGRID || shape == SHAPE_TRIP_RS_OFFGRID_ACC;
+         shape == SHAPE_TRIP_RS_OFFGRID;
 }
 
 enum Kind {
@@ -659,9 +657,9 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (!rs) return launch_ar<DT, OP, false, ShapeS4>(a, grid, s);
       }
       break;
-    case SHAPE_RS2:
-      if constexpr (!ACC32 && Elem<DT>::kSize == 2 && OP != OP_MIN && OP != OP_MAX) {
-        if (rs) return launch_rs<DT, OP, false, ShapeRS2>(a, grid, s);
+    case SHAPE_RS2:  // fp16/bf16 sum/avg/prod, with or without fp32 partials
+      if constexpr (Elem<DT>::kSize == 2 && OP != OP_MIN && OP != OP_MAX) {
+        if (rs) return launch_rs<DT, OP, ACC32, ShapeRS2>(a, grid, s);
       }
       break;
     case SHAPE_RS6:
@@ -693,8 +691,8 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (rs) return launch_rs<DT, OP, false, ShapeRS2, true>(a, grid, s);
       }
       break;
-    case SHAPE_RS_OFFGRID_M:
-      if (rs) return launch_rs<DT, OP, ACC32, ShapeM, true>(a, grid, s);
+    case SHAPE_RS_OFFGRID_M:  // fp32 partials, shards off the vector grid
+      if (rs) return launch_rs<DT, OP, ACC32, ShapeRS2, true>(a, grid, s);
       break;
     case SHAPE_M3:
       if (!rs) return launch_ar<DT, OP, ACC32, ShapeM3>(a, grid, s);
@@ -733,11 +731,6 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (rs) return launch_rs<DT, OP, false, TripS, true, true>(a, grid, s);
       }
       break;
-    case SHAPE_TRIP_RS_OFFGRID_ACC:
-      if constexpr (ACC32) {
-        if (rs) return launch_rs<DT, OP, true, TripRS1, true, true>(a, grid, s);
-      }
-      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -767,7 +760,7 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_W: return shape_params_of<ShapeW>(threads, unroll, min_blocks);
     case SHAPE_RS_OFFGRID: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
     case SHAPE_RS_OFFGRID_B2: return shape_params_of<ShapeRS2>(threads, unroll, min_blocks);
-    case SHAPE_RS_OFFGRID_M: return shape_params_of<ShapeM>(threads, unroll, min_blocks);
+    case SHAPE_RS_OFFGRID_M: return shape_params_of<ShapeRS2>(threads, unroll, min_blocks);
     case SHAPE_M3: return shape_params_of<ShapeM3>(threads, unroll, min_blocks);
     case SHAPE_S4: return shape_params_of<ShapeS4>(threads, unroll, min_blocks);
     case SHAPE_RS2: return shape_params_of<ShapeRS2>(threads, unroll, min_blocks);
@@ -780,7 +773,6 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_TRIP_ACC: return shape_params_of<TripS>(threads, unroll, min_blocks);
     case SHAPE_TRIP_ACC_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
     case SHAPE_TRIP_RS_OFFGRID: return shape_params_of<TripS>(threads, unroll, min_blocks);
-    case SHAPE_TRIP_RS_OFFGRID_ACC: return shape_params_of<TripRS1>(threads, unroll, min_blocks);
     default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
   }
 }

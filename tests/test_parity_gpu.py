@@ -356,7 +356,7 @@ def test_offgrid_compact_buffers_many_tiles(ra, dtype, n):
 @pytest.mark.parametrize("n", [3, 8, 12])
 def test_offgrid_shards_fp32_partials(ra, n):
     # reduce-scatter with fp32 partials into bf16 shards at every 2-byte phase against the vector
-    # grid (the cooperative off-grid stores; one wave at N = 3, a CTA per trip from N = 8)
+    # grid: the off-grid stores realigned in registers, on the one-wave kernel
     dtype = "bf16"
     per_vec = ra.ra_vector_bytes() // ELEM_SIZE[dtype]
     length = n * 128 * per_vec * 3 + 13
