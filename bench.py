@@ -781,6 +781,7 @@ def run_roofs(args):
     probe.rp_store.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_size_t,
                                ctypes.c_void_p]
     probe.rp_load.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
+    probe.rp_copy.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     torch.cuda.set_device(0)
     dev = torch.cuda.current_device()
     peak, peak_kind = measured_peaks()
@@ -845,6 +846,15 @@ def run_roofs(args):
     timed(store(1, [big]), total, "store stream, one-shot CTAs (write 4 GiB)")
     timed(load(0, big), total, "load stream, persistent CTAs (read 4 GiB)")
     timed(load(1, big), total, "load stream, one-shot CTAs (read 4 GiB)")
+    for one_shot, style in ((0, "persistent"), (1, "one-shot")):
+        timed(lambda: check(probe.rp_copy(one_shot, big.data_ptr(), other.data_ptr(), total // 2, stream.cuda_stream)),
+              total, f"copy, {style} CTAs (read 2 GiB + write 2 GiB)")
+    n8, l8 = 8, (256 << 20) // 4
+    s8 = [torch.randn(l8, device="cuda") for _ in range(n8)]
+    r8 = [torch.empty_like(x) for x in s8]
+    timed(lambda: ra.ra_allreduce(s8, r8, "avg", stream=stream), 2 * n8 * l8 * 4,
+          "library all-reduce, N = 8, fp32 avg, 256 MiB per rank (the bench workload)", {"nranks": n8})
+    del s8, r8
     for n in (8, 16):
         bufs = [big[r * (total // n):(r + 1) * (total // n)] for r in range(n)]
         timed(store(0, bufs), total, f"store stream to {n} buffers, persistent CTAs (write 4 GiB)")

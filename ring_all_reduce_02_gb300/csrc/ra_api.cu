@@ -584,7 +584,9 @@ ra_status_t bucket_plan(const size_t* counts, int nparams, size_t bucket_bytes, 
 }
 
 // The all-reduces of buckets [first, first + k) of the table in one launch (k >= 2):
-// ring order, register engine; `whole` holds the checked N whole buffers.
+// ring order, register engine; `whole` holds the checked N whole buffers. From
+// N = 3 on all SMs the group takes a CTA per trip of every bucket's chunk, like
+// a single all-reduce; otherwise one resident wave walks the buckets in turn.
 ra_status_t launch_group(const ra::Args& whole, int dtype, int op, int accum, int max_sms, const size_t* bucket_begin,
                          const size_t* bucket_count, const int* members, int k, void* stream) {
   ra::GroupArgs g;
@@ -601,15 +603,34 @@ ra_status_t launch_group(const ra::Args& whole, int dtype, int op, int accum, in
              op != RA_MAX)
                 ? 1
                 : 0;
-  a.shape = shape_for(a.nranks, false, a.acc32 != 0, dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
-                      op == RA_MIN || op == RA_MAX);
-  // the bucket loop needs a few more registers than ShapeS and ShapeM3 budget (a shape
-  // changes how fast, never which bits)
-  if (a.shape == ra::SHAPE_S || a.shape == ra::SHAPE_M3) a.shape = ra::SHAPE_M;
-  a.count = total;  // sizes the grid like one all-reduce of the group's elements
+  const int n = a.nranks;
+  const int trip = trip_shape_for(ra::KIND_ALLREDUCE, n, elem_size(dtype), a.acc32 != 0, op == RA_MIN || op == RA_MAX,
+                                  false, max_sms);
   dim3 grid;
-  const ra_status_t st = grid_for(a, dtype, a.shape, max_sms, &grid);
-  if (st != RA_SUCCESS) return st;
+  if (trip >= 0) {
+    // every trip of TripS is 128 vectors of a chunk; a bucket's chunks have at most len / n + 1
+    // elements, and its last CTA also takes the edge elements, so it has at least one
+    const uint64_t per_trip = (uint64_t)ra::TripS::kThreads * ra::TripS::kUnroll;
+    const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
+    uint64_t trips = 0;
+    for (int i = 0; i < k; ++i) {
+      g.trip_begin[i] = (uint32_t)trips;
+      trips += (g.count[i] / (uint64_t)n + 1) / v / per_trip + 1;
+      if (trips > 0x7fffffffull) return RA_ERR_UNSUPPORTED;
+    }
+    g.trip_begin[k] = (uint32_t)trips;
+    a.shape = trip;
+    grid = dim3((unsigned)trips, (unsigned)n);
+  } else {
+    a.shape = shape_for(n, false, a.acc32 != 0, dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
+                        op == RA_MIN || op == RA_MAX);
+    // the bucket loop needs a few more registers than ShapeS and ShapeM3 budget (a shape
+    // changes how fast, never which bits)
+    if (a.shape == ra::SHAPE_S || a.shape == ra::SHAPE_M3) a.shape = ra::SHAPE_M;
+    a.count = total;  // sizes the grid like one all-reduce of the group's elements
+    const ra_status_t st = grid_for(a, dtype, a.shape, max_sms, &grid);
+    if (st != RA_SUCCESS) return st;
+  }
   const cudaError_t err = ra::launch_group_kernel(dtype, op, g, grid, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
 }

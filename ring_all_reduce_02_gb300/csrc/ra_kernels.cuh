@@ -448,6 +448,8 @@ struct GroupArgs {
   uint32_t nbuckets;  // 1..kMaxGroup
   uint64_t begin[kMaxGroup];
   uint64_t count[kMaxGroup];
+  // one-trip launches: bucket b owns the CTAs [trip_begin[b], trip_begin[b + 1]) of every row
+  uint32_t trip_begin[kMaxGroup + 1];
 };
 
 template <int DT, int OP, bool ACC32, class SH>
@@ -602,6 +604,63 @@ cudaError_t launch_fused_shape(int kind, const Args& a, dim3 grid, cudaStream_t 
   return kind == KIND_ALLREDUCE ? launch_ar<DT, OP, ACC32, SH>(a, grid, s) : launch_rs<DT, OP, ACC32, SH>(a, grid, s);
 }
 
+// The grouped all-reduce with a CTA per trip: CTA x of row c finds its bucket
+// b (the last with trip_begin[b] <= x), takes trip x - trip_begin[b] of chunk
+// c of that bucket (a CTA-sized block of its vectors), and the bucket's last
+// CTA also takes the chunk's edge elements. Each bucket keeps its own chunk
+// bounds, so its bits are those of a launch of its own.
+template <int DT, int OP, bool ACC32, class SH>
+__global__ void __launch_bounds__(SH::kThreads, SH::kMinBlocks)
+    ar_group_trip_kernel(const __grid_constant__ GroupArgs g) {
+  pdl_enter();
+  constexpr int kThreads = SH::kThreads, kUnroll = SH::kUnroll;
+  constexpr int V = Elem<DT>::kPerVec;
+  constexpr int ES = Elem<DT>::kSize;
+  const Args& a = g.a;
+  const int n = a.nranks, c = blockIdx.y;
+  const uint32_t x = blockIdx.x;
+  uint32_t lo = 0, hi = g.nbuckets;  // trip_begin[lo] <= x < trip_begin[hi]
+  while (hi - lo > 1) {
+    const uint32_t mid = (lo + hi) / 2;
+    if (g.trip_begin[mid] <= x) lo = mid;
+    else hi = mid;
+  }
+  const uint32_t b = lo;
+  const uint64_t t = x - g.trip_begin[b];
+  const uint64_t at = g.begin[b], len = g.count[b];
+  const uint64_t b0 = at + chunk_begin(c, n, len), b1 = at + chunk_begin(c + 1, n, len);
+  uint64_t vb = b0, ve = b0;
+  if (a.vec_ok) vec_range(b0, b1, (uint64_t)a.head, (uint64_t)a.align_elems, V, &vb, &ve);
+  const uint64_t nv = (ve - vb) / V;
+  const uint64_t j0 = t * kThreads * kUnroll + threadIdx.x;
+  if (j0 < nv) {
+    uint64_t off[kUnroll];
+    bool ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint64_t j = j0 + (uint64_t)u * kThreads;
+      ok[u] = j < nv;
+      off[u] = (vb + j * V) * ES;
+    }
+    Vec acc[kUnroll];
+    fold<DT, OP, ACC32, kUnroll, SH::kBatch>(a, c, n, off, ok, acc);
+    for (int r = 0; r < n; ++r) {
+      char* q = static_cast<char*>(a.dst[r]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (ok[u]) st_vec(q + off[u], acc[u]);
+    }
+  }
+  if (x + 1 == g.trip_begin[b + 1]) {  // the bucket's last CTA: the chunk's edge elements
+    const uint64_t n_lo = vb - b0, total = n_lo + (b1 - ve);
+    for (uint64_t k = threadIdx.x; k < total; k += kThreads) {
+      const uint64_t i = k < n_lo ? b0 + k : ve + (k - n_lo);
+      const uint32_t v = fold_elem<DT, OP, ACC32>(a, c, n, i);
+      for (int r = 0; r < n; ++r) st_elem<DT>(a.dst[r], i, v);
+    }
+  }
+}
+
 template <int DT, int OP, bool ACC32, class SH>
 cudaError_t launch_group_shape(const GroupArgs& g, dim3 grid, cudaStream_t s) {
   return launch_programmatic(ar_group_kernel<DT, OP, ACC32, SH>, grid, SH::kThreads, 0, s, g);
@@ -626,6 +685,9 @@ cudaError_t launch_group_fused(const GroupArgs& g, dim3 grid, cudaStream_t s) {
         return launch_group_shape<DT, OP, false, ShapeMB8>(g, grid, s);
       break;
     case SHAPE_W8: return launch_group_shape<DT, OP, ACC32, ShapeW8>(g, grid, s);
+    case SHAPE_TRIP_S:
+    case SHAPE_TRIP_ACC:
+      return launch_programmatic(ar_group_trip_kernel<DT, OP, ACC32, TripS>, grid, TripS::kThreads, 0, s, g);
   }
   return cudaErrorInvalidValue;
 }

@@ -8,7 +8,9 @@
 //  - one-shot: one CTA per 16 KB piece, which it reads or writes and exits,
 //    the style of the library's one-trip kernels and of its all-gather.
 // The store probes write the same piece to each of n destinations (n = 1: a
-// plain store stream; n > 1: the all-gather's write pattern without its reads).
+// plain store stream; n > 1: the all-gather's write pattern without its reads);
+// the copy probes read a piece and write it elsewhere (the 1:1 mix of an
+// all-reduce's traffic).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -65,6 +67,36 @@ __global__ void __launch_bounds__(kThreads) load_one_shot(const char* src, uint3
   if (acc == 0x5bd1e995u) *sink = acc;
 }
 
+__global__ void __launch_bounds__(kThreads) copy_persistent(const char* src, char* dst, uint64_t nvec) {
+  const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+  for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < nvec; i += stride) {
+    uint32_t a, b, c, d, e, f, g, h;
+    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d), "=r"(e), "=r"(f), "=r"(g), "=r"(h)
+                 : "l"(src + i * 32));
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + i * 32), "r"(a), "r"(b), "r"(c),
+                 "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) copy_one_shot(const char* src, char* dst) {
+  const uint64_t i0 = (uint64_t)blockIdx.x * (kPiece / 32) + threadIdx.x;
+  uint32_t v[2][8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[h][0]), "=r"(v[h][1]), "=r"(v[h][2]), "=r"(v[h][3]), "=r"(v[h][4]), "=r"(v[h][5]),
+                   "=r"(v[h][6]), "=r"(v[h][7])
+                 : "l"(src + (i0 + h * kThreads) * 32));
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + (i0 + h * kThreads) * 32),
+                 "r"(v[h][0]), "r"(v[h][1]), "r"(v[h][2]), "r"(v[h][3]), "r"(v[h][4]), "r"(v[h][5]), "r"(v[h][6]),
+                 "r"(v[h][7])
+                 : "memory");
+}
+
 int persistent_grid() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -114,6 +146,25 @@ int rp_load(int one_shot, const void* src, size_t bytes, void* sink, void* strea
     const int grid = persistent_grid();
     if (grid <= 0) return (int)cudaErrorUnknown;
     load_persistent<<<grid, kThreads, 0, s>>>(p, bytes / 32, k);
+  }
+  return (int)cudaGetLastError();
+}
+
+// Copies `bytes` (a nonzero multiple of 16 KB) from device buffer src to dst (not
+// overlapping): the 1:1 mix of reads and writes. Returns a cudaError_t.
+int rp_copy(int one_shot, const void* src, void* dst, size_t bytes, void* stream) {
+  if (src == nullptr || dst == nullptr || bytes == 0 || bytes % kPiece) return (int)cudaErrorInvalidValue;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const char* p = static_cast<const char*>(src);
+  char* q = static_cast<char*>(dst);
+  if (one_shot) {
+    const uint64_t pieces = bytes / kPiece;
+    if (pieces > 0x7fffffffull) return (int)cudaErrorInvalidValue;
+    copy_one_shot<<<(unsigned)pieces, kThreads, 0, s>>>(p, q);
+  } else {
+    const int grid = persistent_grid();
+    if (grid <= 0) return (int)cudaErrorUnknown;
+    copy_persistent<<<grid, kThreads, 0, s>>>(p, q, bytes / 32);
   }
   return (int)cudaGetLastError();
 }
