@@ -429,7 +429,9 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 }
 
 // The one-trip shape for a fused call, or -1 to keep the one-wave shape:
-// all-reduces from N = 3, reduce-scatters from N = 8 and, for 4-byte types,
+// TripW at N <= 2 (for a reduce-scatter only when every shard is on the vector
+// grid: shards stored in 4-byte units were not measured there), TripS and the
+// like for all-reduces from N = 3, reduce-scatters from N = 8 and, for 4-byte types,
 // from N = 4 (fp32 avg, 1 GiB over all ranks: 105-107% against 101-105%; bf16
 // lost 3-4 points there), fp32 partials and shards off the vector grid
 // included, but not both at once (bf16 avg at N = 12, 1 GiB: 96.7% one-wave
@@ -439,18 +441,22 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 #ifndef RA_GRID_MODE
 #define RA_GRID_MODE -1
 #endif
-int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax, bool offgrid, int max_sms) {
+int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax, bool offgrid, bool shards_on_grid,
+                   int max_sms) {
   if (max_sms > 0 || kind == ra::KIND_ALLGATHER) return -1;
   const bool rs = kind == ra::KIND_REDUCE_SCATTER;
   if (rs && offgrid && acc32) return -1;
+  const bool small_n = nranks <= 2 && !acc32 && (!rs || shards_on_grid);
   int trip;
-  if (rs && offgrid) trip = ra::SHAPE_TRIP_RS_OFFGRID;
+  if (small_n) trip = ra::SHAPE_TRIP_W;
+  else if (rs && offgrid) trip = ra::SHAPE_TRIP_RS_OFFGRID;
   else if (acc32) trip = rs ? ra::SHAPE_TRIP_ACC_RS2 : ra::SHAPE_TRIP_ACC;
   else trip = (rs && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S;
 #if RA_GRID_MODE >= 0
   (void)nranks, (void)elem_bytes;
   return RA_GRID_MODE == 1 ? trip : -1;
 #else
+  if (small_n) return trip;
   if (rs) return (nranks >= 8 || (elem_bytes == 4 && nranks >= 4)) ? trip : -1;
   return nranks >= 3 ? trip : -1;
 #endif
@@ -501,8 +507,10 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   if (offgrid)
     a.shape = a.acc32 ? ra::SHAPE_RS_OFFGRID_M
                       : (a.shape == ra::SHAPE_S ? ra::SHAPE_RS_OFFGRID : ra::SHAPE_RS_OFFGRID_B2);
-  const int trip =
-      trip_shape_for(kind, nranks, elem_size(dtype), a.acc32 != 0, op == RA_MIN || op == RA_MAX, offgrid, max_sms);
+  const uint64_t all_chunks = nranks >= 64 ? ~0ull : ((1ull << nranks) - 1);
+  const bool shards_on_grid = a.vec_ok && (a.compact_aligned & all_chunks) == all_chunks;
+  const int trip = trip_shape_for(kind, nranks, elem_size(dtype), a.acc32 != 0, op == RA_MIN || op == RA_MAX,
+                                  offgrid, shards_on_grid, max_sms);
   if (trip >= 0) a.shape = trip;
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
@@ -604,8 +612,10 @@ ra_status_t launch_group(const ra::Args& whole, int dtype, int op, int accum, in
                 ? 1
                 : 0;
   const int n = a.nranks;
-  const int trip = trip_shape_for(ra::KIND_ALLREDUCE, n, elem_size(dtype), a.acc32 != 0, op == RA_MIN || op == RA_MAX,
-                                  false, max_sms);
+  // the grouped kernel has one-trip instances on TripS only (N >= 3); N <= 2 keeps one wave
+  int trip = trip_shape_for(ra::KIND_ALLREDUCE, n, elem_size(dtype), a.acc32 != 0, op == RA_MIN || op == RA_MAX,
+                            false, true, max_sms);
+  if (trip == ra::SHAPE_TRIP_W) trip = -1;
   dim3 grid;
   if (trip >= 0) {
     // every trip of TripS is 128 vectors of a chunk; a bucket's chunks have at most len / n + 1

@@ -156,6 +156,14 @@ using ShapeW8 = ShapeS;
 // (101.9 / 103.3% at N = 8 / 16 against 96.1 / 98.4%; TripS would spill there).
 using TripS = Shape<128, 8, 1, 4>;
 using TripRS2 = Shape<128, 4, 2, 4>;
+// N <= 2 has too few loads per thread on TripS to keep HBM busy; 128 x 2 at 8
+// CTAs/SM with loads of 2 ranks, from five candidates (fp32 and bf16, avg and
+// max, N = 1, 2, back to back): all-reduce 104-105.5% at 1 GiB over all ranks,
+// 101.5-104% at 256 MiB, 94-102.5% at 64 MiB, against 98-100%, 96-96.6% and
+// 86-90% on the one-wave shapes; reduce-scatter 104.7-106.9% at 1 GiB against
+// 95.7-100%. At N = 3 the all-reduce already takes TripS, and a reduce-scatter
+// on this shape lost 20 points to one wave (fp32, shards off the vector grid).
+using TripW = Shape<128, 8, 2, 2>;
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
 // vector grid at a 2-byte offset, on ShapeS, or on ShapeRS2 (where the plain
 // call would take loads of 2 ranks at a time; _M: with fp32 partials).
@@ -179,12 +187,13 @@ enum ShapeId {
   SHAPE_TRIP_RS2 = 16,  // TripRS2, one trip per CTA (reduce-scatter min/max)
   SHAPE_TRIP_ACC = 17,  // TripS, one trip per CTA, fp32 partials (all-reduce)
   SHAPE_TRIP_ACC_RS2 = 18,  // TripRS2, one trip per CTA, fp32 partials (reduce-scatter)
-  SHAPE_TRIP_RS_OFFGRID = 19  // TripS, one trip per CTA, reduce-scatter with 2-byte-offset shards
+  SHAPE_TRIP_RS_OFFGRID = 19,  // TripS, one trip per CTA, reduce-scatter with 2-byte-offset shards
+  SHAPE_TRIP_W = 20            // TripW, one trip per CTA (N <= 2)
 };
 // A launch that takes a CTA per trip instead of one resident wave.
 __host__ __device__ constexpr bool is_trip_shape(int shape) {
   return shape == SHAPE_TRIP_S || shape == SHAPE_TRIP_RS2 || shape == SHAPE_TRIP_ACC || shape == SHAPE_TRIP_ACC_RS2 ||
-         shape == SHAPE_TRIP_RS_OFFGRID;
+         shape == SHAPE_TRIP_RS_OFFGRID || shape == SHAPE_TRIP_W;
 }
 
 enum Kind {
@@ -793,6 +802,12 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (rs) return launch_rs<DT, OP, false, TripS, true, true>(a, grid, s);
       }
       break;
+    case SHAPE_TRIP_W:
+      if constexpr (!ACC32) {
+        if (rs) return launch_rs<DT, OP, false, TripW, false, true>(a, grid, s);
+        return launch_ar<DT, OP, false, TripW, true>(a, grid, s);
+      }
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -835,6 +850,7 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_TRIP_ACC: return shape_params_of<TripS>(threads, unroll, min_blocks);
     case SHAPE_TRIP_ACC_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
     case SHAPE_TRIP_RS_OFFGRID: return shape_params_of<TripS>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_W: return shape_params_of<TripW>(threads, unroll, min_blocks);
     default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
   }
 }
