@@ -612,15 +612,15 @@ ra_status_t launch_group(const ra::Args& whole, int dtype, int op, int accum, in
                 ? 1
                 : 0;
   const int n = a.nranks;
-  // the grouped kernel has one-trip instances on TripS only (N >= 3); N <= 2 keeps one wave
-  int trip = trip_shape_for(ra::KIND_ALLREDUCE, n, elem_size(dtype), a.acc32 != 0, op == RA_MIN || op == RA_MAX,
-                            false, true, max_sms);
-  if (trip == ra::SHAPE_TRIP_W) trip = -1;
+  const int trip = trip_shape_for(ra::KIND_ALLREDUCE, n, elem_size(dtype), a.acc32 != 0,
+                                  op == RA_MIN || op == RA_MAX, false, true, max_sms);
   dim3 grid;
   if (trip >= 0) {
-    // every trip of TripS is 128 vectors of a chunk; a bucket's chunks have at most len / n + 1
-    // elements, and its last CTA also takes the edge elements, so it has at least one
-    const uint64_t per_trip = (uint64_t)ra::TripS::kThreads * ra::TripS::kUnroll;
+    // every trip is threads x vectors of a chunk (TripS: 128, TripW: 256); a bucket's chunks have
+    // at most len / n + 1 elements, and its last CTA also takes the edge elements, so it has at
+    // least one
+    const uint64_t per_trip = trip == ra::SHAPE_TRIP_W ? (uint64_t)ra::TripW::kThreads * ra::TripW::kUnroll
+                                                       : (uint64_t)ra::TripS::kThreads * ra::TripS::kUnroll;
     const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
     uint64_t trips = 0;
     for (int i = 0; i < k; ++i) {

@@ -697,6 +697,10 @@ cudaError_t launch_group_fused(const GroupArgs& g, dim3 grid, cudaStream_t s) {
     case SHAPE_TRIP_S:
     case SHAPE_TRIP_ACC:
       return launch_programmatic(ar_group_trip_kernel<DT, OP, ACC32, TripS>, grid, TripS::kThreads, 0, s, g);
+    case SHAPE_TRIP_W:
+      if constexpr (!ACC32)
+        return launch_programmatic(ar_group_trip_kernel<DT, OP, false, TripW>, grid, TripW::kThreads, 0, s, g);
+      break;
   }
   return cudaErrorInvalidValue;
 }
