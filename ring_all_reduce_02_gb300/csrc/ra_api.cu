@@ -436,6 +436,9 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 // lost 3-4 points there), fp32 partials and shards off the vector grid
 // included, but not both at once (bf16 avg at N = 12, 1 GiB: 96.7% one-wave
 // against 90.0%), on every SM (an SM budget caps the grid by definition).
+// Min/max reduce-scatters take TripRS2 on and off the grid (bf16 min/max with
+// 2-byte-offset shards, N = 9..15, 1 GiB: 102.3-104.5% against 94.6-100.3% on
+// TripS).
 // RA_GRID_MODE, a build-time tunable for sweeps: -1 this rule, 0 never, 1
 // wherever a trip shape exists.
 #ifndef RA_GRID_MODE
@@ -449,7 +452,7 @@ int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax
   const bool small_n = nranks <= 2 && !acc32 && (!rs || shards_on_grid);
   int trip;
   if (small_n) trip = ra::SHAPE_TRIP_W;
-  else if (rs && offgrid) trip = ra::SHAPE_TRIP_RS_OFFGRID;
+  else if (rs && offgrid) trip = minmax ? ra::SHAPE_TRIP_RS2_OFFGRID : ra::SHAPE_TRIP_RS_OFFGRID;
   else if (acc32) trip = rs ? ra::SHAPE_TRIP_ACC_RS2 : ra::SHAPE_TRIP_ACC;
   else trip = (rs && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S;
 #if RA_GRID_MODE >= 0

@@ -353,6 +353,29 @@ def test_offgrid_compact_buffers_many_tiles(ra, dtype, n):
             assert_same_bits(to_host(recvs[c].view, dtype), want[c], dtype, f"AG off {off} rank {c}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("op", ["min", "max"])
+@pytest.mark.parametrize("n", [3, 9, 12])
+def test_offgrid_shards_min_max(ra, dtype, op, n):
+    # min/max reduce-scatters into 16-bit shards at odd and even phases against the vector grid,
+    # several trips per chunk: the min/max launch shapes with the realigned off-grid stores
+    per_vec = ra.ra_vector_bytes() // ELEM_SIZE[dtype]
+    length = n * 512 * per_vec + 29
+    xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=110 + n)
+    shards_want, _ = oracle.reduce_scatter(xs, op, dtype)
+    bounds = [oracle.chunk_range(length, n, c) for c in range(n)]
+    for off in (0, 1, 2, 5, per_vec - 1):
+        sends = [Padded(length, dtype) for _ in range(n)]
+        for b, x in zip(sends, xs):
+            b.fill(x)
+        outs = [Padded(e - b, dtype, (off + c) % per_vec) for c, (b, e) in enumerate(bounds)]
+        ra.ra_reduce_scatter([b.view for b in sends], [o.view for o in outs], op)
+        torch.cuda.synchronize()
+        for c in range(n):
+            assert outs[c].canaries_intact(), f"off {off} chunk {c}"
+            assert_same_bits(to_host(outs[c].view, dtype), shards_want[c], dtype, f"off {off} chunk {c}")
+
+
 @pytest.mark.parametrize("n", [3, 8, 12])
 def test_offgrid_shards_fp32_partials(ra, n):
     # reduce-scatter with fp32 partials into bf16 shards at every 2-byte phase against the vector
