@@ -429,9 +429,9 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 }
 
 // The one-trip shape for a fused call, or -1 to keep the one-wave shape:
-// TripW at N <= 2 (for a reduce-scatter only when every shard is on the vector
-// grid: shards stored in 4-byte units were not measured there), TripS and the
-// like for all-reduces from N = 3, reduce-scatters from N = 8 and, for 4-byte types,
+// TripW at small N (below; for a reduce-scatter only when every shard is on
+// the vector grid: with shards stored in 4-byte units it lost up to 25 points),
+// TripS and the like for all-reduces from N = 3, reduce-scatters from N = 8 and, for 4-byte types,
 // from N = 4 (fp32 avg, 1 GiB over all ranks: 105-107% against 101-105%; bf16
 // lost 3-4 points there), fp32 partials and shards off the vector grid
 // included, but not both at once (bf16 avg at N = 12, 1 GiB: 96.7% one-wave
@@ -449,7 +449,13 @@ int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax
   if (max_sms > 0 || kind == ra::KIND_ALLGATHER) return -1;
   const bool rs = kind == ra::KIND_REDUCE_SCATTER;
   if (rs && offgrid && acc32) return -1;
-  const bool small_n = nranks <= 2 && !acc32 && (!rs || shards_on_grid);
+  // TripW: all-reduces at N <= 2; reduce-scatters whose shards all sit on the vector grid at
+  // N <= 4, and at N = 5..7 for 16-bit types and float min/max (1 GiB over all ranks: 106-108.7%
+  // against 100.4-104.8%; 256 MiB: 97.7-103% against 96-102.7%). 4-byte sums at N = 5..7 measured
+  // the same at 1 GiB and up to 4 points lower at 256 MiB, and every call from N = 8 up to 5 points
+  // lower at 256 MiB, so those keep TripS / TripRS2.
+  const bool small_n =
+      !acc32 && (rs ? shards_on_grid && (nranks <= 4 || (nranks <= 7 && (elem_bytes == 2 || minmax))) : nranks <= 2);
   int trip;
   if (small_n) trip = ra::SHAPE_TRIP_W;
   else if (rs && offgrid) trip = minmax ? ra::SHAPE_TRIP_RS2_OFFGRID : ra::SHAPE_TRIP_RS_OFFGRID;

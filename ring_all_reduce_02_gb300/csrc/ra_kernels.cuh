@@ -162,7 +162,9 @@ using TripRS2 = Shape<128, 4, 2, 4>;
 // 101.5-104% at 256 MiB, 94-102.5% at 64 MiB, against 98-100%, 96-96.6% and
 // 86-90% on the one-wave shapes; reduce-scatter 104.7-106.9% at 1 GiB against
 // 95.7-100%. At N = 3 the all-reduce already takes TripS, and a reduce-scatter
-// on this shape lost 20 points to one wave (fp32, shards off the vector grid).
+// on this shape lost 20 points to one wave (fp32, shards off the vector grid);
+// with every shard on the grid, reduce-scatters take it up to N = 4, and up to
+// N = 7 for 16-bit types and float min/max (106-108.7% at 1 GiB).
 using TripW = Shape<128, 8, 2, 2>;
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
 // vector grid at a 2-byte offset, on ShapeS, or on ShapeRS2 (where the plain
@@ -188,7 +190,7 @@ enum ShapeId {
   SHAPE_TRIP_ACC = 17,  // TripS, one trip per CTA, fp32 partials (all-reduce)
   SHAPE_TRIP_ACC_RS2 = 18,  // TripRS2, one trip per CTA, fp32 partials (reduce-scatter)
   SHAPE_TRIP_RS_OFFGRID = 19,  // TripS, one trip per CTA, reduce-scatter with 2-byte-offset shards
-  SHAPE_TRIP_W = 20,           // TripW, one trip per CTA (N <= 2)
+  SHAPE_TRIP_W = 20,           // TripW, one trip per CTA (small N)
   SHAPE_TRIP_RS2_OFFGRID = 21  // TripRS2, one trip per CTA, min/max reduce-scatter with 2-byte-offset shards
 };
 // A launch that takes a CTA per trip instead of one resident wave.
