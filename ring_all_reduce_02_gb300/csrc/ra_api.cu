@@ -445,7 +445,7 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 #define RA_GRID_MODE -1
 #endif
 int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax, bool offgrid, bool shards_on_grid,
-                   int max_sms) {
+                   uint64_t total_bytes, int max_sms) {
   if (max_sms > 0 || kind == ra::KIND_ALLGATHER) return -1;
   const bool rs = kind == ra::KIND_REDUCE_SCATTER;
   if (rs && offgrid && acc32) return -1;
@@ -466,6 +466,13 @@ int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax
   return RA_GRID_MODE == 1 ? trip : -1;
 #else
   if (small_n) return trip;
+  // 16-bit sum/avg/prod with 2-byte-offset shards at N = 5..7 stream best on TripW from about
+  // 384 MiB over all ranks (bf16 avg / fp16 sum at 1 GiB: 102.5-104.8% against 97.2-100.5%; at
+  // 512 MiB +2.8-4.6 points at N = 6, 7 and level at 5; at 384 MiB +0.3-1.8), one wave below that
+  // (at 256 MiB TripW lost 4 points at N = 5, at 128 MiB 3-6 points) and at N = 3 (it lost 2-16
+  // points at every size)
+  if (rs && offgrid && elem_bytes == 2 && !minmax && nranks >= 5 && nranks <= 7 && total_bytes >= (320ull << 20))
+    return ra::SHAPE_TRIP_W_OFFGRID;
   if (rs) return (nranks >= 8 || (elem_bytes == 4 && nranks >= 4)) ? trip : -1;
   return nranks >= 3 ? trip : -1;
 #endif
@@ -523,7 +530,7 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   // IEEE minimum/maximum of the float types keeps TripRS2 (TripS: 92.5-105.4% against 99.0-106.8%)
   const bool minmax_shape = (op == RA_MIN || op == RA_MAX) && dtype != RA_INT32;
   const int trip = trip_shape_for(kind, nranks, elem_size(dtype), a.acc32 != 0, minmax_shape, offgrid,
-                                  shards_on_grid, max_sms);
+                                  shards_on_grid, (uint64_t)nranks * count * (uint64_t)elem_size(dtype), max_sms);
   if (trip >= 0) a.shape = trip;
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
@@ -626,7 +633,7 @@ ra_status_t launch_group(const ra::Args& whole, int dtype, int op, int accum, in
                 : 0;
   const int n = a.nranks;
   const int trip = trip_shape_for(ra::KIND_ALLREDUCE, n, elem_size(dtype), a.acc32 != 0,
-                                  op == RA_MIN || op == RA_MAX, false, true, max_sms);
+                                  op == RA_MIN || op == RA_MAX, false, true, 0, max_sms);
   dim3 grid;
   if (trip >= 0) {
     // every trip is threads x vectors of a chunk (TripS: 128, TripW: 256); a bucket's chunks have

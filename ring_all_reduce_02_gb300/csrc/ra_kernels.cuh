@@ -191,12 +191,14 @@ enum ShapeId {
   SHAPE_TRIP_ACC_RS2 = 18,  // TripRS2, one trip per CTA, fp32 partials (reduce-scatter)
   SHAPE_TRIP_RS_OFFGRID = 19,  // TripS, one trip per CTA, reduce-scatter with 2-byte-offset shards
   SHAPE_TRIP_W = 20,           // TripW, one trip per CTA (small N)
-  SHAPE_TRIP_RS2_OFFGRID = 21  // TripRS2, one trip per CTA, min/max reduce-scatter with 2-byte-offset shards
+  SHAPE_TRIP_RS2_OFFGRID = 21,  // TripRS2, one trip per CTA, min/max reduce-scatter with 2-byte-offset shards
+  SHAPE_TRIP_W_OFFGRID = 22     // TripW, one trip per CTA, 16-bit reduce-scatter with 2-byte-offset shards
 };
 // A launch that takes a CTA per trip instead of one resident wave.
 __host__ __device__ constexpr bool is_trip_shape(int shape) {
   return shape == SHAPE_TRIP_S || shape == SHAPE_TRIP_RS2 || shape == SHAPE_TRIP_ACC || shape == SHAPE_TRIP_ACC_RS2 ||
-         shape == SHAPE_TRIP_RS_OFFGRID || shape == SHAPE_TRIP_W || shape == SHAPE_TRIP_RS2_OFFGRID;
+         shape == SHAPE_TRIP_RS_OFFGRID || shape == SHAPE_TRIP_W || shape == SHAPE_TRIP_RS2_OFFGRID ||
+         shape == SHAPE_TRIP_W_OFFGRID;
 }
 
 enum Kind {
@@ -814,6 +816,11 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
         if (rs) return launch_rs<DT, OP, false, TripRS2, true, true>(a, grid, s);
       }
       break;
+    case SHAPE_TRIP_W_OFFGRID:
+      if constexpr (!ACC32 && Elem<DT>::kSize == 2 && OP != OP_MIN && OP != OP_MAX) {
+        if (rs) return launch_rs<DT, OP, false, TripW, true, true>(a, grid, s);
+      }
+      break;
     case SHAPE_TRIP_W:
       if constexpr (!ACC32) {
         if (rs) return launch_rs<DT, OP, false, TripW, false, true>(a, grid, s);
@@ -864,6 +871,7 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_TRIP_RS_OFFGRID: return shape_params_of<TripS>(threads, unroll, min_blocks);
     case SHAPE_TRIP_W: return shape_params_of<TripW>(threads, unroll, min_blocks);
     case SHAPE_TRIP_RS2_OFFGRID: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_W_OFFGRID: return shape_params_of<TripW>(threads, unroll, min_blocks);
     default: return shape_params_of<ShapeS>(threads, unroll, min_blocks);
   }
 }

@@ -562,6 +562,27 @@ def test_full_size_n8_bf16_avg_gpt2m(ra):
     check_full_size(ra, n, length, dtype, op, dist, rs_ag=True)
 
 
+@pytest.mark.parametrize("n,dtype,op", [(6, "bf16", "avg"), (7, "f16", "sum")])
+def test_offgrid_16bit_reduce_scatter_from_512_mib(ra, n, dtype, op):
+    # 16-bit reduce-scatters with shards off the vector grid at N = 5..7 take a one-trip launch
+    # from 320 MiB over all ranks: every element of every shard against the oracle's ring
+    length = (512 << 20) // ELEM_SIZE[dtype] // n + 5
+    if _host_ram_gb() < 3 * n * length * ELEM_SIZE[dtype] / 2**30 + 4:
+        pytest.skip("host RAM too small")
+    xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=130 + n)
+    sends = [to_device(x, dtype) for x in xs]
+    bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+    shards = [torch.empty(e - b, dtype=TORCH_DTYPE[dtype], device="cuda") for b, e in bounds]
+    ra.ra_reduce_scatter(sends, shards, op)
+    torch.cuda.synchronize()
+    del sends
+    assert any((b * ELEM_SIZE[dtype]) % ra.ra_vector_bytes() for b, _ in bounds), "no shard off the grid"
+    want, _ = oracle.reduce_scatter(xs, op, dtype, timeout_ms=ORACLE_TIMEOUT_MS)
+    del xs
+    for c in range(n):
+        same_bits_fast(to_host(shards[c], dtype), want[c], dtype, f"n={n} shard {c}")
+
+
 def test_full_size_n8_bf16_avg_gpt2m_fp32_partials(ra):
     # the same bucket with fp32 partials, rounded once: every element against the oracle's ring
     # whose messages are fp32
