@@ -428,18 +428,22 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
   return err == cudaSuccess ? RA_SUCCESS : cuda_failed(err);
 }
 
-// The one-trip shape for a fused call, or -1 to keep the one-wave shape:
-// TripW at small N (below; for a reduce-scatter only when every shard is on
-// the vector grid: with shards stored in 4-byte units it lost up to 25 points),
-// TripS and the like for all-reduces from N = 3, reduce-scatters from N = 8 and, for 4-byte types,
-// from N = 4 (fp32 avg, 1 GiB over all ranks: 105-107% against 101-105%; bf16
-// lost 3-4 points there), fp32 partials and shards off the vector grid
-// included, but not both at once (bf16 avg at N = 12, 1 GiB: 96.7% one-wave
-// against 90.0%), on every SM (an SM budget caps the grid by definition).
-// Min/max reduce-scatters take TripRS2 on and off the grid (bf16 min/max with
-// 2-byte-offset shards, N = 9..15, 1 GiB: 102.3-104.5% against 94.6-100.3% on
-// TripS).
-// RA_GRID_MODE, a build-time tunable for sweeps: -1 this rule, 0 never, 1
+// The one-trip shape for a fused call, or -1 to keep the one-wave shape, on
+// every SM (an SM budget caps the grid by definition). minmax: a float min/max
+// (int32 min/max fold as cheaply as sums and take the sum shapes). Each rule
+// below is the measured winner (back to back, 1 GiB and 256 MiB over all ranks):
+// - TripW at small N: all-reduces at N <= 2; reduce-scatters whose shards all
+//   sit on the vector grid at N <= 4, and at N = 5..7 for 16-bit types and
+//   float min/max (shards stored in 4-byte units lost up to 25 points on it);
+// - TripS for all-reduces from N = 3, and for reduce-scatters from N = 8 and,
+//   for 4-byte types, from N = 4 (fp32 avg at 1 GiB: 105-107% against 101-105%;
+//   bf16 lost 3-4 points there); TripRS2 for float min/max reduce-scatters,
+//   on and off the grid (bf16 with 2-byte-offset shards, N = 9..15: 102.3-104.5%
+//   against 94.6-100.3% on TripS);
+// - fp32 partials and shards off the vector grid take trips too, but not both
+//   at once (bf16 avg at N = 12: 96.7% one-wave against 90.0%);
+// - large 16-bit off-grid sums at N = 5..7 (below).
+// RA_GRID_MODE, a build-time tunable for sweeps: -1 these rules, 0 never, 1
 // wherever a trip shape exists.
 #ifndef RA_GRID_MODE
 #define RA_GRID_MODE -1
@@ -462,7 +466,7 @@ int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax
   else if (acc32) trip = rs ? ra::SHAPE_TRIP_ACC_RS2 : ra::SHAPE_TRIP_ACC;
   else trip = (rs && minmax) ? ra::SHAPE_TRIP_RS2 : ra::SHAPE_TRIP_S;
 #if RA_GRID_MODE >= 0
-  (void)nranks, (void)elem_bytes;
+  (void)nranks, (void)elem_bytes, (void)total_bytes;
   return RA_GRID_MODE == 1 ? trip : -1;
 #else
   if (small_n) return trip;
