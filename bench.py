@@ -782,6 +782,7 @@ def run_roofs(args):
                                ctypes.c_void_p]
     probe.rp_load.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
     probe.rp_copy.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    probe.rp_copy_sms.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
     torch.cuda.set_device(0)
     dev = torch.cuda.current_device()
     peak, peak_kind = measured_peaks()
@@ -805,7 +806,7 @@ def run_roofs(args):
     def load(one_shot, buf):
         return lambda: check(probe.rp_load(one_shot, buf.data_ptr(), buf.numel(), sink.data_ptr(), stream.cuda_stream))
 
-    def timed(fn, nbytes, label, extra=None):
+    def timed(fn, nbytes, label, extra=None, sms=0):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -833,6 +834,9 @@ def run_roofs(args):
                "clean_GBps": round(nbytes / statistics.median(clean) / GB, 1),
                "b2b_GBps": round(nbytes / b2b / GB, 1),
                "b2b_frac_of_copy_peak": round(nbytes / b2b / GB / peak, 4), "peak": f"{peak} ({peak_kind})"}
+        if sms:
+            rec["sms"] = sms
+            rec["b2b_GBps_per_sm"] = round(nbytes / b2b / GB / sms, 1)
         rec.update(extra or {})
         print(json.dumps(rec), flush=True)
 
@@ -854,6 +858,20 @@ def run_roofs(args):
     r8 = [torch.empty_like(x) for x in s8]
     timed(lambda: ra.ra_allreduce(s8, r8, "avg", stream=stream), 2 * n8 * l8 * 4,
           "library all-reduce, N = 8, fp32 avg, 256 MiB per rank (the bench workload)", {"nranks": n8})
+    # what a share of the SMs can move: a plain copy on k CTAs of 1024 threads (one per SM), and the
+    # library's all-reduce on an SM budget of k with either engine
+    bstat = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for k in (16, 32, 64):
+        nb = k * (16 << 20)
+        timed(lambda: check(probe.rp_copy_sms(big.data_ptr(), other.data_ptr(), nb // 2, k, stream.cuda_stream)),
+              nb, f"copy on {k} SMs (one 1024-thread CTA per SM)", sms=k)
+        for engine in ("registers", "bulk"):
+            timed(lambda: ra.ra_allreduce_ex(s8, r8, "avg", max_sms=k, engine=engine,
+                                             status=bstat if engine == "bulk" else None, stream=stream),
+                  2 * n8 * l8 * 4, f"library all-reduce on {k} SMs, {engine} engine, N = 8, fp32 avg, 256 MiB per rank",
+                  {"nranks": n8}, sms=k)
+    if bstat.item() != 0:
+        raise RuntimeError(f"bulk engine reported status {bstat.item()}")
     del s8, r8
     for n in (8, 16):
         bufs = [big[r * (total // n):(r + 1) * (total // n)] for r in range(n)]

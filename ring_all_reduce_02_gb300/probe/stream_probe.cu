@@ -10,7 +10,8 @@
 // The store probes write the same piece to each of n destinations (n = 1: a
 // plain store stream; n > 1: the all-gather's write pattern without its reads);
 // the copy probes read a piece and write it elsewhere (the 1:1 mix of an
-// all-reduce's traffic).
+// all-reduce's traffic). The SM-share copy runs on a given number of CTAs, one
+// per SM, to show how many bytes a share of the SMs can move.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -97,6 +98,29 @@ __global__ void __launch_bounds__(kThreads) copy_one_shot(const char* src, char*
                  : "memory");
 }
 
+// one CTA of kShareThreads per SM-share slot: CTA b copies bytes [b * slab, (b + 1) * slab)
+constexpr int kShareThreads = 1024;
+__global__ void __launch_bounds__(kShareThreads) copy_share(const char* src, char* dst, uint64_t slab) {
+  const char* s = src + blockIdx.x * slab;
+  char* d = dst + blockIdx.x * slab;
+  const uint64_t nvec = slab / 32;
+  for (uint64_t i = threadIdx.x; i < nvec; i += 4 * kShareThreads) {
+    uint32_t v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                   : "=r"(v[u][0]), "=r"(v[u][1]), "=r"(v[u][2]), "=r"(v[u][3]), "=r"(v[u][4]), "=r"(v[u][5]),
+                     "=r"(v[u][6]), "=r"(v[u][7])
+                   : "l"(s + (i + (uint64_t)u * kShareThreads) * 32));
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d + (i + (uint64_t)u * kShareThreads) * 32),
+                   "r"(v[u][0]), "r"(v[u][1]), "r"(v[u][2]), "r"(v[u][3]), "r"(v[u][4]), "r"(v[u][5]), "r"(v[u][6]),
+                   "r"(v[u][7])
+                   : "memory");
+  }
+}
+
 int persistent_grid() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -166,6 +190,17 @@ int rp_copy(int one_shot, const void* src, void* dst, size_t bytes, void* stream
     if (grid <= 0) return (int)cudaErrorUnknown;
     copy_persistent<<<grid, kThreads, 0, s>>>(p, q, bytes / 32);
   }
+  return (int)cudaGetLastError();
+}
+
+// Copies `bytes` from src to dst on `ctas` CTAs of 1024 threads (one per SM
+// while ctas <= the SM count): the copy rate an SM share reaches. bytes must be
+// a nonzero multiple of ctas * 128 KB. Returns a cudaError_t.
+int rp_copy_sms(const void* src, void* dst, size_t bytes, int ctas, void* stream) {
+  if (src == nullptr || dst == nullptr || ctas < 1 || bytes == 0 || bytes % ((size_t)ctas * 4 * kShareThreads * 32))
+    return (int)cudaErrorInvalidValue;
+  copy_share<<<ctas, kShareThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const char*>(src), static_cast<char*>(dst), bytes / (size_t)ctas);
   return (int)cudaGetLastError();
 }
 

@@ -35,6 +35,15 @@ def test_library_exports_every_declared_symbol(ra):
     assert set(ra.EXPORTS) == set(names)
 
 
+def test_stream_probes_build_and_export(ra):
+    # the measurement kernels behind bench.py --roofs (not the collective path)
+    from ring_all_reduce_02_gb300 import build
+
+    probe = ctypes.CDLL(build.build_probe())
+    for name in ("rp_store", "rp_load", "rp_copy", "rp_copy_sms"):
+        assert hasattr(probe, name), name
+
+
 def test_chunk_range_is_floor_definition(ra):
     for n in range(1, 65):
         for count in list(range(0, 40)) + [1003, 1_000_003, 354_823_168, 1 << 28, (1 << 57) - 1]:
