@@ -533,8 +533,10 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   // 1 GiB over all ranks, N = 4..16: 104.7-107.9% on TripS against 99.5-106.9% on TripRS2); the
   // IEEE minimum/maximum of the float types keeps TripRS2 (TripS: 92.5-105.4% against 99.0-106.8%)
   const bool minmax_shape = (op == RA_MIN || op == RA_MAX) && dtype != RA_INT32;
+  const uint64_t rank_bytes = (uint64_t)count * (uint64_t)elem_size(dtype);  // <= 2^59
+  const uint64_t total_bytes = rank_bytes > UINT64_MAX / (uint64_t)nranks ? UINT64_MAX : rank_bytes * (uint64_t)nranks;
   const int trip = trip_shape_for(kind, nranks, elem_size(dtype), a.acc32 != 0, minmax_shape, offgrid,
-                                  shards_on_grid, (uint64_t)nranks * count * (uint64_t)elem_size(dtype), max_sms);
+                                  shards_on_grid, total_bytes, max_sms);
   if (trip >= 0) a.shape = trip;
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
