@@ -353,6 +353,27 @@ def test_offgrid_compact_buffers_many_tiles(ra, dtype, n):
             assert_same_bits(to_host(recvs[c].view, dtype), want[c], dtype, f"AG off {off} rank {c}")
 
 
+@pytest.mark.parametrize("dtype,op", list(itertools.product(DTYPES, OPS)))
+def test_ongrid_shards_small_n(ra, dtype, op):
+    # reduce-scatters whose shards all sit on the vector grid (L a multiple of N vectors, shards in
+    # their own allocations) at N = 1..8: the small-N one-trip launches (N <= 4, and up to 7 for
+    # 16-bit types and float min/max), several trips per chunk plus a partial one
+    per_vec = ra.ra_vector_bytes() // ELEM_SIZE[dtype]
+    for n in range(1, 9):
+        length = n * per_vec * (2 * 256 + 37)
+        xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=150 + n)
+        shards_want, _ = oracle.reduce_scatter(xs, op, dtype)
+        sends = [to_device(x, dtype) for x in xs]
+        bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+        assert all((b * ELEM_SIZE[dtype]) % ra.ra_vector_bytes() == 0 for b, _ in bounds)
+        shards = [Padded(e - b, dtype) for b, e in bounds]
+        ra.ra_reduce_scatter(sends, [s.view for s in shards], op)
+        torch.cuda.synchronize()
+        for c in range(n):
+            assert shards[c].canaries_intact(), f"n={n} chunk {c}"
+            assert_same_bits(to_host(shards[c].view, dtype), shards_want[c], dtype, f"n={n} shard {c}")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("op", ["min", "max"])
 @pytest.mark.parametrize("n", [3, 9, 12])
