@@ -298,14 +298,17 @@ ra_status_t plan_bulk(const ra::Args& a, int dtype, int op, int max_sms, BulkLau
   b.withhold_chunk = -1;
   const int n = a.nranks;
   // about 32 KB per stage: 32 KB / N per rank, between 4 and 16 KB (fewer, longer tiles when N
-  // is small, so the per-tile barrier work is spread over more bytes), and at least one vector
-  // per consumer thread
+  // is small, so the per-tile barrier work is spread over more bytes), and one vector per consumer
+  // thread where two stages still fit
   uint32_t tile_bytes = 32768u / (uint32_t)n;
   if (tile_bytes < 4096u) tile_bytes = 4096u;
   if (tile_bytes > 16384u) tile_bytes = 16384u;
   uint32_t tv = tile_bytes / (uint32_t)ra::kVecBytes;
   tv = tv / ra::kBulkConsumers * ra::kBulkConsumers;
   if (tv < (uint32_t)ra::kBulkConsumers) tv = ra::kBulkConsumers;
+  // keep at least two stages: shrink the tile to a multiple of a warp's vectors (some consumer
+  // threads then idle on each tile)
+  while (tv > 32 && 2 * (size_t)n * tv * ra::kVecBytes > kBulkSmemBudget) tv -= 32;
   b.tile_vecs = tv;
   const size_t stage_bytes = (size_t)n * b.tile_vecs * ra::kVecBytes;
   size_t stages = kBulkSmemBudget / stage_bytes;

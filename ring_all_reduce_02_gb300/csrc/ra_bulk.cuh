@@ -22,7 +22,16 @@
 
 namespace ra {
 
-constexpr int kBulkConsumers = 128;               // folding threads (4 warps)
+// Folding threads (12 warps). More consumers keep more stores in flight, which
+// is what bounds an SM budget: N = 8 fp32 avg, 256 MiB per rank, on 16 / 32 / 64
+// SMs, GB/s per SM with 128 / 256 / 384 / 512 consumers: 87 / 89 / 92 / 91,
+// 88 / 89 / 89 / 90, 87 / 89 / 87 / 87; at N = 2: 54 / 83 / 89 / 104; at N = 3:
+// 59 / 84 / 98 / 99; at N = 4: 78 / 104 / 105 / 100; at N = 16: 88 / 95 / 95 /
+// 94 on 16 SMs and 86-88 on 64. 384 is the best compromise.
+#ifndef RA_BULK_CONSUMERS
+#define RA_BULK_CONSUMERS 384
+#endif
+constexpr int kBulkConsumers = RA_BULK_CONSUMERS;
 constexpr int kBulkThreads = kBulkConsumers + 32;  // + one producer warp
 constexpr uint64_t kWaitNs = 1000000000ull;       // 1 s per wait
 constexpr int kBulkErrFull = 1;                    // a stage's bulk copies did not land in time
@@ -32,7 +41,7 @@ struct BulkArgs {
   Args base;
   int* status;        // device words; 0 = fine, else the first error code seen
   uint32_t status_stride;  // 0: every chunk reports into status[0]; 1: chunk c into status[c]
-  uint32_t tile_vecs;  // vectors per rank per stage (a multiple of kBulkConsumers)
+  uint32_t tile_vecs;  // vectors per rank per stage (a multiple of 32)
   uint32_t stages;     // stages in the shared-memory ring
   int withhold_chunk;  // self-test of the bounded waits: -1 none, else CTA (0, c) never issues its
                        // first tile's copies for c = withhold_chunk
