@@ -297,6 +297,12 @@ ra_status_t plan_bulk(const ra::Args& a, int dtype, int op, int max_sms, BulkLau
   b.status_stride = 0;
   b.withhold_chunk = -1;
   const int n = a.nranks;
+  int sms = 0, all_sms = 0;
+  ra_status_t st = sm_budget(max_sms, &sms);
+  if (st == RA_SUCCESS) st = sm_budget(0, &all_sms);
+  if (st != RA_SUCCESS) return st;
+  const uint32_t nc = (uint32_t)ra::bulk_consumers_for(n, sms < all_sms);
+  b.consumers = nc;
   // about 32 KB per stage: 32 KB / N per rank, between 4 and 16 KB (fewer, longer tiles when N
   // is small, so the per-tile barrier work is spread over more bytes), and one vector per consumer
   // thread where two stages still fit
@@ -304,8 +310,8 @@ ra_status_t plan_bulk(const ra::Args& a, int dtype, int op, int max_sms, BulkLau
   if (tile_bytes < 4096u) tile_bytes = 4096u;
   if (tile_bytes > 16384u) tile_bytes = 16384u;
   uint32_t tv = tile_bytes / (uint32_t)ra::kVecBytes;
-  tv = tv / ra::kBulkConsumers * ra::kBulkConsumers;
-  if (tv < (uint32_t)ra::kBulkConsumers) tv = ra::kBulkConsumers;
+  tv = tv / nc * nc;
+  if (tv < nc) tv = nc;
   // keep at least two stages: shrink the tile to a multiple of a warp's vectors (some consumer
   // threads then idle on each tile)
   while (tv > 32 && 2 * (size_t)n * tv * ra::kVecBytes > kBulkSmemBudget) tv -= 32;
@@ -316,9 +322,6 @@ ra_status_t plan_bulk(const ra::Args& a, int dtype, int op, int max_sms, BulkLau
   if (stages < 2) return RA_ERR_UNSUPPORTED;
   b.stages = (uint32_t)stages;
   p->smem = 128 * ((2 * stages * 8 + 127) / 128) + stages * stage_bytes;
-  int sms = 0;
-  const ra_status_t st = sm_budget(max_sms, &sms);
-  if (st != RA_SUCCESS) return st;
   const uint64_t v = (uint64_t)(ra::kVecBytes / elem_size(dtype));
   const uint64_t tiles = ((a.count + n - 1) / n / v) / b.tile_vecs + 1;
   uint64_t gx = (uint64_t)sms / (uint64_t)n;

@@ -22,17 +22,20 @@
 
 namespace ra {
 
-// Folding threads (12 warps). More consumers keep more stores in flight, which
-// is what bounds an SM budget: N = 8 fp32 avg, 256 MiB per rank, on 16 / 32 / 64
-// SMs, GB/s per SM with 128 / 256 / 384 / 512 consumers: 87 / 89 / 92 / 91,
-// 88 / 89 / 89 / 90, 87 / 89 / 87 / 87; at N = 2: 54 / 83 / 89 / 104; at N = 3:
-// 59 / 84 / 98 / 99; at N = 4: 78 / 104 / 105 / 100; at N = 16: 88 / 95 / 95 /
-// 94 on 16 SMs and 86-88 on 64. 384 is the best compromise.
-#ifndef RA_BULK_CONSUMERS
-#define RA_BULK_CONSUMERS 384
-#endif
-constexpr int kBulkConsumers = RA_BULK_CONSUMERS;
-constexpr int kBulkThreads = kBulkConsumers + 32;  // + one producer warp
+// Folding threads per CTA, chosen per launch (BulkArgs::consumers). More
+// consumers keep more stores in flight, which is what bounds an SM budget: N = 8
+// fp32 avg, 256 MiB per rank, on 16 / 32 / 64 SMs, GB/s per SM with 128 / 256 /
+// 384 / 512 consumers: 87 / 89 / 92 / 91, 88 / 89 / 89 / 90, 87 / 89 / 87 / 87;
+// at N = 2: 54 / 83 / 89 / 104; at N = 3: 59 / 84 / 98 / 99; at N = 4: 78 / 104
+// / 105 / 100; at N = 16: 88 / 95 / 95 / 94 on 16 SMs and 86-88 on 64. On all
+// SMs 384 gained at N <= 4 (37-42 against 42-43 GB/s per SM) and lost 1.5% at
+// N = 8 and 16. So: 384 on an SM budget or below N = 8, else 128.
+// The two counts are separate instantiations: 384 as a launch-time value
+// measured 9 points below the instantiated 384 at N = 16 on SM budgets.
+constexpr int kBulkConsumersWide = 384, kBulkConsumersNarrow = 128;
+inline int bulk_consumers_for(int nranks, bool sm_budget) {
+  return (sm_budget || nranks < 8) ? kBulkConsumersWide : kBulkConsumersNarrow;
+}
 constexpr uint64_t kWaitNs = 1000000000ull;       // 1 s per wait
 constexpr int kBulkErrFull = 1;                    // a stage's bulk copies did not land in time
 constexpr int kBulkErrEmpty = 2;                   // the consumers did not release a stage in time
@@ -42,6 +45,8 @@ struct BulkArgs {
   int* status;        // device words; 0 = fine, else the first error code seen
   uint32_t status_stride;  // 0: every chunk reports into status[0]; 1: chunk c into status[c]
   uint32_t tile_vecs;  // vectors per rank per stage (a multiple of 32)
+  uint32_t consumers;  // folding threads: kBulkConsumersWide or kBulkConsumersNarrow; the CTA has
+                       // consumers + 32 threads (the last warp is the producer's)
   uint32_t stages;     // stages in the shared-memory ring
   int withhold_chunk;  // self-test of the bounded waits: -1 none, else CTA (0, c) never issues its
                        // first tile's copies for c = withhold_chunk
@@ -88,14 +93,15 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
 }
 __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(status, 0, code); }
 
-template <int DT, int OP>
-__global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_constant__ BulkArgs ba) {
+template <int DT, int OP, int NC>
+__global__ void __launch_bounds__(NC + 32, 1) ar_bulk_kernel(const __grid_constant__ BulkArgs ba) {
   pdl_enter();
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int V = Elem<DT>::kPerVec;
   constexpr int ES = Elem<DT>::kSize;
   const Args& a = ba.base;
   const int n = a.nranks, c = blockIdx.y;
+  constexpr uint32_t NT = NC + 32;
   const uint32_t S = ba.stages, TV = ba.tile_vecs;
   const uint32_t tile_bytes = TV * kVecBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [S]: bulk copies of a stage landed
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kBulkConsumers / 32);
+      mbar_init(&empty[s], NC / 32);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -121,9 +127,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
   __syncthreads();
 
   const uint64_t first = blockIdx.x, step = gridDim.x;
-  if (threadIdx.x >= kBulkConsumers) {
+  if (threadIdx.x >= NC) {
     // ---- producer warp: one elected thread issues the bulk copies --------------
-    if (threadIdx.x == kBulkConsumers) {
+    if (threadIdx.x == NC) {
       uint32_t issued = 0;
       for (uint64_t t = first; t < ntiles; t += step, ++issued) {
         const uint32_t s = issued % S;
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
         break;
       }
       const uint8_t* tile = data + (size_t)s * n * tile_bytes;
-      for (uint32_t j = threadIdx.x; j < TV; j += kBulkConsumers) {
+      for (uint32_t j = threadIdx.x; j < TV; j += NC) {
         Vec acc = *reinterpret_cast<const Vec*>(tile + (size_t)j * kVecBytes);  // slot 0 = rank c
         for (int k = 1; k < n; ++k)
           acc = vec_hop<DT, OP>(acc, *reinterpret_cast<const Vec*>(tile + (size_t)k * tile_bytes + j * kVecBytes));
@@ -174,8 +180,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
 
   // the part of the chunk outside whole tiles, read directly: leftover vectors, then edge elements
   const uint64_t tail_beg = ntiles * TV;
-  for (uint64_t j = tail_beg + (uint64_t)blockIdx.x * kBulkThreads + threadIdx.x; j < nv;
-       j += (uint64_t)gridDim.x * kBulkThreads) {
+  for (uint64_t j = tail_beg + (uint64_t)blockIdx.x * NT + threadIdx.x; j < nv; j += (uint64_t)gridDim.x * NT) {
     const uint64_t off = (vb + j * V) * ES;
     Vec acc = ld_vec(static_cast<const char*>(a.src[c]) + off);
     for (int k = 1; k < n; ++k) {
@@ -186,22 +191,34 @@ __global__ void __launch_bounds__(kBulkThreads, 1) ar_bulk_kernel(const __grid_c
     if constexpr (OP == OP_AVG) acc = vec_avg<DT>(acc, a.inv_n, n);
     for (int r = 0; r < n; ++r) st_vec(static_cast<char*>(a.dst[r]) + off, acc);
   }
-  for_each_edge_elem<kBulkThreads>(b0, vb, ve, b1, [&](uint64_t i) {
+  const uint64_t n_lo = vb - b0, n_edge = n_lo + (b1 - ve);  // edge elements (the CTA width is per launch)
+  for (uint64_t k = (uint64_t)(gridDim.x - 1 - blockIdx.x) * NT + threadIdx.x; k < n_edge;
+       k += (uint64_t)gridDim.x * NT) {
+    const uint64_t i = k < n_lo ? b0 + k : ve + (k - n_lo);
     const uint32_t v = fold_elem<DT, OP, false>(a, c, n, i);
     for (int r = 0; r < n; ++r) st_elem<DT>(a.dst[r], i, v);
-  });
+  }
 }
 
-// Raises the kernel's dynamic shared-memory limit to `smem`; enqueues nothing.
+// Raises both instances' dynamic shared-memory limit to `smem`; enqueues nothing.
 template <int DT, int OP>
 cudaError_t configure_bulk_op(size_t smem) {
-  return cudaFuncSetAttribute(ar_bulk_kernel<DT, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t err = cudaFuncSetAttribute(ar_bulk_kernel<DT, OP, kBulkConsumersWide>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  return cudaFuncSetAttribute(ar_bulk_kernel<DT, OP, kBulkConsumersNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
 }
 
 // Launches the kernel; configure_bulk_op(smem) must have succeeded on this device.
 template <int DT, int OP>
 cudaError_t launch_bulk_op(const BulkArgs& b, dim3 grid, size_t smem, cudaStream_t s) {
-  return launch_programmatic(ar_bulk_kernel<DT, OP>, grid, kBulkThreads, smem, s, b);
+  if (b.consumers == (uint32_t)kBulkConsumersWide)
+    return launch_programmatic(ar_bulk_kernel<DT, OP, kBulkConsumersWide>, grid, kBulkConsumersWide + 32, smem, s, b);
+  if (b.consumers == (uint32_t)kBulkConsumersNarrow)
+    return launch_programmatic(ar_bulk_kernel<DT, OP, kBulkConsumersNarrow>, grid, kBulkConsumersNarrow + 32, smem, s,
+                               b);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ra

@@ -911,8 +911,10 @@ def test_sm_budget_changes_nothing_but_speed(ra):
                                       ("i32", "max"), ("bf16", "min")])
 def test_bulk_engine(ra, dtype, op):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # 384 consumer threads on an SM budget or below N = 8, else 128; from N = 9 on a budget the tiles
+    # shrink below one vector per consumer so that two stages fit
     for n, length in ((1, 100), (2, 1 << 16), (3, 3 * 4096 * 7 + 11), (5, 1003), (8, (1 << 20) + 13),
-                      (16, 16 * 2048 * 5 + 3)):
+                      (12, 12 * 4096 * 5 + 7), (16, 16 * 2048 * 5 + 3)):
         xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=n + 90)
         want, _, _ = oracle.allreduce(xs, op, dtype)
         for max_sms, inplace in ((0, False), (16, False), (0, True)):
