@@ -149,7 +149,11 @@ typedef struct {
   ra_accum_t accum;   /* RA_ACCUM_DTYPE by default */
   int max_sms;        /* 0: the launch may fill every SM; k > 0: at most k SMs' worth of CTAs, leaving the
                          rest to work running beside the collective (arjunsriva.com "AllReduce, All the
-                         Way Down": communication kernels compete with compute for SMs) */
+                         Way Down": communication kernels compete with compute for SMs). The hardware
+                         places the CTAs: the budget bounds the collective's share of CTA slots, not
+                         which SMs it runs on, and a launch shape with several CTAs per SM may spread
+                         over more than k SMs (the bulk engine runs one CTA per SM); a hard partition
+                         of the SMs needs green contexts */
   ra_engine_t engine; /* RA_ENGINE_REGISTERS by default */
   int* status;        /* RA_ENGINE_BULK only: one int of device memory, owned by the caller, that the
                          kernel sets to a nonzero code if one of its bounded waits gives up (1: a
