@@ -788,6 +788,8 @@ def run_roofs(args):
     probe.rp_load.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
     probe.rp_copy.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     probe.rp_copy_sms.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    probe.rp_copy_n.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_size_t,
+                                ctypes.c_void_p]
     torch.cuda.set_device(0)
     dev = torch.cuda.current_device()
     peak, peak_kind = measured_peaks()
@@ -882,6 +884,11 @@ def run_roofs(args):
         bufs = [big[r * (total // n):(r + 1) * (total // n)] for r in range(n)]
         timed(store(0, bufs), total, f"store stream to {n} buffers, persistent CTAs (write 4 GiB)")
         timed(store(1, bufs), total, f"store stream to {n} buffers, one-shot CTAs (write 4 GiB)")
+        # the all-gather's mix: each piece read once from `other` and written to the n buffers
+        piece = total // n
+        arr = (ctypes.c_void_p * n)(*[b.data_ptr() for b in bufs])
+        timed(lambda: check(probe.rp_copy_n(other.data_ptr(), arr, n, piece, stream.cuda_stream)), piece + total,
+              f"read once, write to {n} buffers, one-shot CTAs (read {piece >> 20} MiB + write 4 GiB)")
         length = (1 << 30) // 4 // n
         bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
         shards = [torch.randn(e - b, device="cuda") for b, e in bounds]

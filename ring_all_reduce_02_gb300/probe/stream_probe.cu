@@ -121,6 +121,27 @@ __global__ void __launch_bounds__(kShareThreads) copy_share(const char* src, cha
   }
 }
 
+// one CTA per 16 KB piece: read it once and write it to each of n destinations
+// (the all-gather's traffic: one read, n writes)
+__global__ void __launch_bounds__(kThreads) copy_n_one_shot(const char* src, const __grid_constant__ Dsts d, int n) {
+  const uint64_t i0 = (uint64_t)blockIdx.x * (kPiece / 32) + threadIdx.x;
+  uint32_t v[2][8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[h][0]), "=r"(v[h][1]), "=r"(v[h][2]), "=r"(v[h][3]), "=r"(v[h][4]), "=r"(v[h][5]),
+                   "=r"(v[h][6]), "=r"(v[h][7])
+                 : "l"(src + (i0 + h * kThreads) * 32));
+  for (int r = 0; r < n; ++r) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d.p[r] + (i0 + h * kThreads) * 32),
+                   "r"(v[h][0]), "r"(v[h][1]), "r"(v[h][2]), "r"(v[h][3]), "r"(v[h][4]), "r"(v[h][5]),
+                   "r"(v[h][6]), "r"(v[h][7])
+                   : "memory");
+  }
+}
+
 int persistent_grid() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -190,6 +211,24 @@ int rp_copy(int one_shot, const void* src, void* dst, size_t bytes, void* stream
     if (grid <= 0) return (int)cudaErrorUnknown;
     copy_persistent<<<grid, kThreads, 0, s>>>(p, q, bytes / 32);
   }
+  return (int)cudaGetLastError();
+}
+
+// Reads `bytes` (a nonzero multiple of 16 KB) of src once and writes them to
+// each of the n (1..64) device buffers dst[0..n), one CTA per 16 KB piece: the
+// traffic mix of an all-gather. Returns a cudaError_t.
+int rp_copy_n(const void* src, void* const* dst, int n, size_t bytes, void* stream) {
+  if (src == nullptr || dst == nullptr || n < 1 || n > kMaxBuffers || bytes == 0 || bytes % kPiece)
+    return (int)cudaErrorInvalidValue;
+  Dsts d{};
+  for (int r = 0; r < n; ++r) {
+    if (dst[r] == nullptr) return (int)cudaErrorInvalidValue;
+    d.p[r] = static_cast<char*>(dst[r]);
+  }
+  const uint64_t pieces = bytes / kPiece;
+  if (pieces > 0x7fffffffull) return (int)cudaErrorInvalidValue;
+  copy_n_one_shot<<<(unsigned)pieces, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const char*>(src), d, n);
   return (int)cudaGetLastError();
 }
 
