@@ -790,6 +790,8 @@ def run_roofs(args):
     probe.rp_copy_sms.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
     probe.rp_copy_n.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_size_t,
                                 ctypes.c_void_p]
+    probe.rp_read_n.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                ctypes.c_void_p]
     torch.cuda.set_device(0)
     dev = torch.cuda.current_device()
     peak, peak_kind = measured_peaks()
@@ -889,6 +891,16 @@ def run_roofs(args):
         arr = (ctypes.c_void_p * n)(*[b.data_ptr() for b in bufs])
         timed(lambda: check(probe.rp_copy_n(other.data_ptr(), arr, n, piece, stream.cuda_stream)), piece + total,
               f"read once, write to {n} buffers, one-shot CTAs (read {piece >> 20} MiB + write 4 GiB)")
+        # the reduce-scatter's mix: each piece read from the n buffers, one combination written to `other`
+        timed(lambda: check(probe.rp_read_n(arr, n, other.data_ptr(), piece, stream.cuda_stream)), total + piece,
+              f"read {n} buffers, write once, one-shot CTAs (read 4 GiB + write {piece >> 20} MiB)")
+        rs_len = (1 << 30) // 4 // n
+        rs_in = [torch.randn(rs_len, device="cuda") for _ in range(n)]
+        rs_bounds = [ra.ra_chunk_range(rs_len, n, c) for c in range(n)]
+        rs_out = [torch.empty(e - b, device="cuda") for b, e in rs_bounds]
+        timed(lambda: ra.ra_reduce_scatter(rs_in, rs_out, "sum", stream=stream), (n + 1) * rs_len * 4,
+              f"library reduce-scatter, N = {n}, fp32 sum, 1 GiB over all ranks", {"nranks": n})
+        del rs_in, rs_out
         length = (1 << 30) // 4 // n
         bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
         shards = [torch.randn(e - b, device="cuda") for b, e in bounds]

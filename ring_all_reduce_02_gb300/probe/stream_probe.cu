@@ -142,6 +142,33 @@ __global__ void __launch_bounds__(kThreads) copy_n_one_shot(const char* src, con
   }
 }
 
+// one CTA per 16 KB piece: read it from each of n sources and write one
+// combination of them (the reduce-scatter's traffic: n reads, one write)
+struct Srcs {
+  const char* p[kMaxBuffers];
+};
+__global__ void __launch_bounds__(kThreads) read_n_one_shot(const __grid_constant__ Srcs sr, int n, char* dst) {
+  const uint64_t i0 = (uint64_t)blockIdx.x * (kPiece / 32) + threadIdx.x;
+  uint32_t acc[2][8] = {};
+  for (int r = 0; r < n; ++r) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[8];
+      asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                   : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                   : "l"(sr.p[r] + (i0 + h * kThreads) * 32));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[h][k] ^= v[k];
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + (i0 + h * kThreads) * 32),
+                 "r"(acc[h][0]), "r"(acc[h][1]), "r"(acc[h][2]), "r"(acc[h][3]), "r"(acc[h][4]), "r"(acc[h][5]),
+                 "r"(acc[h][6]), "r"(acc[h][7])
+                 : "memory");
+}
+
 int persistent_grid() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -229,6 +256,23 @@ int rp_copy_n(const void* src, void* const* dst, int n, size_t bytes, void* stre
   if (pieces > 0x7fffffffull) return (int)cudaErrorInvalidValue;
   copy_n_one_shot<<<(unsigned)pieces, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const char*>(src), d, n);
+  return (int)cudaGetLastError();
+}
+
+// Reads `bytes` (a nonzero multiple of 16 KB) from each of the n (1..64)
+// device buffers src[0..n) and writes one combination of them to dst, one CTA
+// per 16 KB piece: the traffic mix of a reduce-scatter. Returns a cudaError_t.
+int rp_read_n(const void* const* src, int n, void* dst, size_t bytes, void* stream) {
+  if (src == nullptr || dst == nullptr || n < 1 || n > kMaxBuffers || bytes == 0 || bytes % kPiece)
+    return (int)cudaErrorInvalidValue;
+  Srcs sr{};
+  for (int r = 0; r < n; ++r) {
+    if (src[r] == nullptr) return (int)cudaErrorInvalidValue;
+    sr.p[r] = static_cast<const char*>(src[r]);
+  }
+  const uint64_t pieces = bytes / kPiece;
+  if (pieces > 0x7fffffffull) return (int)cudaErrorInvalidValue;
+  read_n_one_shot<<<(unsigned)pieces, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(sr, n, static_cast<char*>(dst));
   return (int)cudaGetLastError();
 }
 

@@ -40,7 +40,7 @@ def test_stream_probes_build_and_export(ra):
     from ring_all_reduce_02_gb300 import build
 
     probe = ctypes.CDLL(build.build_probe())
-    for name in ("rp_store", "rp_load", "rp_copy", "rp_copy_sms", "rp_copy_n"):
+    for name in ("rp_store", "rp_load", "rp_copy", "rp_copy_sms", "rp_copy_n", "rp_read_n"):
         assert hasattr(probe, name), name
 
 
