@@ -218,27 +218,26 @@ def test_ring_order_is_reproduced(ra):
         assert_same_bits(got[3], want[3], "f32", f"chunk {c}")
 
 
-@pytest.mark.parametrize("length", [4 * 15 + 11, 5 * 4096 + 11])
+@pytest.mark.parametrize("length", [4 * 15 + 11, 5 * 4096 + 11, 8 * 16 * 100])
 def test_special_values(ra, length):
     # NaN, infinities, signed zeros, subnormals in every float dtype; the short length runs on the
-    # per-element edge path, the long one on the vector path (paired 16-bit min/max, off-grid
-    # compact reduce-scatter outputs and all-gather inputs)
+    # per-element edge path, the long ones on the vector path (paired 16-bit min/max, off-grid
+    # compact reduce-scatter outputs and all-gather inputs; at 12800 every shard is on the vector
+    # grid), at N = 2, 5 and 8 (the small-N, all-reduce and reduce-scatter launch shapes)
     specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-40, 6e-8, -6e-8, 1e-39, 65504.0,
                          -65504.0, 3.4e38, 1.0, -1.0], dtype=np.float32)
     rng = np.random.default_rng(3)
-    for dtype in ("f32", "f16", "bf16"):
-        for op in OPS:
-            n = 5
-            xs = []
-            for r in range(n):
-                v = rng.choice(specials, size=length).astype(np.float32)
-                if dtype == "f16":
-                    xs.append(v.astype(np.float16))
-                elif dtype == "bf16":
-                    xs.append(oracle.round_f32("bf16", v))
-                else:
-                    xs.append(v)
-            check_all(ra, xs, op, dtype, f"specials {dtype} {op} L={length}")
+    for dtype, op, n in itertools.product(("f32", "f16", "bf16"), OPS, (2, 5, 8)):
+        xs = []
+        for r in range(n):
+            v = rng.choice(specials, size=length).astype(np.float32)
+            if dtype == "f16":
+                xs.append(v.astype(np.float16))
+            elif dtype == "bf16":
+                xs.append(oracle.round_f32("bf16", v))
+            else:
+                xs.append(v)
+        check_all(ra, xs, op, dtype, f"specials {dtype} {op} N={n} L={length}")
 
 
 def test_int32_wrap_and_avg(ra):
@@ -269,6 +268,24 @@ def test_inplace_equals_out_of_place(ra, dtype):
     g2 = run_allgather(ra, s1, length, dtype, inplace=True)
     for r in range(n):
         assert g1[r].tobytes() == g2[r].tobytes() == a[0].tobytes()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_inplace_small_n_on_grid(ra, dtype):
+    # in place with every shard on the vector grid at small N: the one-trip launches of N <= 2
+    # all-reduces and of on-grid reduce-scatters up to N = 7 read and write the same buffers
+    per_vec = ra.ra_vector_bytes() // ELEM_SIZE[dtype]
+    for n in (1, 2, 3, 4, 6, 7):
+        length = n * per_vec * 300
+        for op in ("sum", "max"):
+            xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=170 + n)
+            want, _, _ = oracle.allreduce(xs, op, dtype)
+            got = run_allreduce(ra, xs, op, dtype, inplace=True)
+            shards = run_reduce_scatter(ra, xs, op, dtype, inplace=True)
+            bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+            for r, (b, e) in enumerate(bounds):
+                assert_same_bits(got[r], want[r], dtype, f"AR in place n={n} {op} rank {r}")
+                assert_same_bits(shards[r], want[0][b:e], dtype, f"RS in place n={n} {op} shard {r}")
 
 
 @pytest.mark.parametrize("n", [3, 5, 12])
