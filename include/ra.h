@@ -49,7 +49,11 @@
  *    (pinned host memory under unified addressing, or any host memory on
  *    systems whose GPU accesses system memory coherently): the kernels then
  *    read and write host memory directly over the host link, which replaces
- *    explicit copies for callers whose data lives on the host.
+ *    explicit copies for callers whose data lives on the host. Such calls
+ *    launch one resident wave (it streams the host link faster than a CTA per
+ *    trip) and the all-gather takes plain stores; the TMA-staged bulk engine
+ *    and the tree / Rabenseifner orders take device memory only and return
+ *    RA_ERR_UNSUPPORTED for a host buffer, before enqueuing anything.
  *  - Buffers must not overlap, except in the exact in-place layout named for
  *    each call (each element is then read and written by the same thread).
  *    Send buffers may overlap each other (they are only read).
@@ -293,8 +297,11 @@ int ra_vector_bytes(void);
  * call of its own to use and would only fragment that pool with a stray
  * cudaMalloc; a caller between the kernels of a training step, where
  * cudaFree would make the host wait for the whole device, including the
- * compute that the bulk engine is meant to run beside; and a host program
- * that all-reduces pinned host buffers and owns no device memory at all.
+ * compute that the bulk engine is meant to run beside; and a caller that
+ * wants the per-chunk codes in pinned host memory (chunk_status may be host
+ * memory). The buffers themselves must be device memory (RA_ERR_UNSUPPORTED
+ * otherwise): a program whose buffers are pinned host memory calls
+ * ra_allreduce, which reads and writes them over the host link.
  *
  * Set-up: every call looks up the array's device address in the current
  * context (cudaGetSymbolAddress) and keeps nothing between calls, so a call

@@ -269,6 +269,26 @@ ra_status_t launch(int kind, int dtype, int op, const ra::Args& a, dim3 grid, vo
 
 const ra_options_t kDefaultOptions = {RA_ORDER_RING, RA_ACCUM_DTYPE, 0, RA_ENGINE_REGISTERS, nullptr};
 
+// Memory the device reaches over the host link: pinned host memory, or pageable
+// host memory on a system whose GPU reads system memory coherently (the
+// runtime reports them as registered and unregistered host memory). Device and
+// managed memory are not. A pointer the runtime cannot describe counts as
+// device memory; its launch then reports any failure of its own.
+bool on_host(const void* p) {
+  if (p == nullptr) return false;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+bool any_on_host(const ra::Args& a) {
+  for (int r = 0; r < a.nranks; ++r)
+    if (on_host(a.src[r]) || on_host(a.dst[r])) return true;
+  return false;
+}
+
 // The bulk engine: tiles of tile_vecs vectors per rank, as many stages as fit
 // in about 200 KB of shared memory (2..8), one CTA per SM on the budget.
 #ifndef RA_BULK_SMEM_KB
@@ -291,6 +311,8 @@ struct BulkLaunch {
 // what it needs. Enqueues nothing: every error the bulk path can report before
 // its launch is reported here.
 ra_status_t plan_bulk(const ra::Args& a, int dtype, int op, int max_sms, BulkLaunch* p) {
+  // the bulk engine's loads are TMA bulk copies, which the library issues on device memory only
+  if (any_on_host(a)) return RA_ERR_UNSUPPORTED;
   ra::BulkArgs& b = p->args;
   b.base = a;
   b.status = nullptr;
@@ -401,6 +423,8 @@ void tree_programs(ra::OrderArgs& o, int n) {
 }
 
 ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int order, int max_sms, void* stream) {
+  // the ordered kernel stages its loads with cp.async, which the library issues on device memory only
+  if (any_on_host(a)) return RA_ERR_UNSUPPORTED;
   ra::OrderArgs o;
   memset(&o, 0, sizeof(o));
   o.base = a;
@@ -524,6 +548,9 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   // kernel's rows of CTAs spread it instead
   int ag_kernel = ra::ag_plan_for(nranks).kernel;
   if (!a.vec_ok) ag_kernel = ra::AG_REGISTERS;
+  // the tile kernel writes with TMA bulk stores, which the library issues on device memory only;
+  // buffers in host memory take the register kernel's plain stores
+  if (kind == ra::KIND_ALLGATHER && ag_kernel == ra::AG_TILE && any_on_host(a)) ag_kernel = ra::AG_REGISTERS;
   a.shape = kind == ra::KIND_ALLGATHER ? ra::kShapeAgBase + ag_kernel
                                        : shape_for(nranks, kind == ra::KIND_REDUCE_SCATTER, a.acc32 != 0,
                                                    dtype == RA_FLOAT16 || dtype == RA_BFLOAT16,
@@ -543,7 +570,11 @@ ra_status_t run(int kind, const void* const* sendbufs, void* const* recvbufs, si
   const uint64_t total_bytes = rank_bytes > UINT64_MAX / (uint64_t)nranks ? UINT64_MAX : rank_bytes * (uint64_t)nranks;
   const int trip = trip_shape_for(kind, nranks, elem_size(dtype), a.acc32 != 0, minmax_shape, offgrid,
                                   shards_on_grid, total_bytes, max_sms);
-  if (trip >= 0) a.shape = trip;
+  // buffers in host memory stream over the host link faster from one resident wave (8 x 256 MiB fp32
+  // avg on pinned host buffers: 335.5 GB/s of link traffic, the rate of concurrent copy-engine
+  // transfers, against 326.9 GB/s with a CTA per trip)
+  const bool host_side = on_host(sendbufs[0]) || on_host(recvbufs[0]);
+  if (trip >= 0 && !host_side) a.shape = trip;
   dim3 grid;
   st = grid_for(a, dtype, a.shape, max_sms, &grid);
   if (st != RA_SUCCESS) return st;

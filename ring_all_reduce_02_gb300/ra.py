@@ -127,8 +127,8 @@ def _stream_ptr(stream) -> int:
 def _check(tensors, what):
     dt = tensors[0].dtype
     for t in tensors:
-        if not t.is_cuda:
-            raise ValueError(f"{what}: every buffer must be a CUDA tensor")
+        if not (t.is_cuda or (t.device.type == "cpu" and t.is_pinned())):
+            raise ValueError(f"{what}: every buffer must be a CUDA tensor or pinned host memory")
         if t.dtype != dt:
             raise ValueError(f"{what}: all buffers must share one dtype")
         if not t.is_contiguous():

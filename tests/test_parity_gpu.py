@@ -288,6 +288,43 @@ def test_inplace_small_n_on_grid(ra, dtype):
                 assert_same_bits(shards[r], want[0][b:e], dtype, f"RS in place n={n} {op} shard {r}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_pinned_host_buffers(ra, dtype):
+    # buffers in pinned host memory, read and written by the kernels over the host link (the bench's
+    # end-to-end leg): all-reduce host -> host and host -> device, reduce-scatter into host shards,
+    # all-gather from host shards into host buffers (plain stores, not the TMA tile kernel), every
+    # element against the oracle; the paths built on TMA or cp.async refuse host memory up front
+    td = TORCH_DTYPE[dtype]
+    for n, length in ((2, 2 * 4096 * 3), (5, 5 * 1003 * 7 + 3), (8, (1 << 18) + 13)):
+        xs = inputs.rank_buffers(n, length, dtype, ("normal", 1.0), seed_base=190 + n)
+        want, _, _ = oracle.allreduce(xs, "avg", dtype)
+        shards_want, _ = oracle.reduce_scatter(xs, "avg", dtype)
+        sends = [to_device(x, dtype).cpu().pin_memory() for x in xs]
+        host_out = [torch.empty(length, dtype=td).pin_memory() for _ in range(n)]
+        dev_out = [torch.empty(length, dtype=td, device="cuda") for _ in range(n)]
+        ra.ra_allreduce(sends, host_out, "avg")
+        ra.ra_allreduce(sends, dev_out, "avg")
+        bounds = [ra.ra_chunk_range(length, n, c) for c in range(n)]
+        shards = [torch.empty(e - b, dtype=td).pin_memory() for b, e in bounds]
+        ra.ra_reduce_scatter(sends, shards, "avg")
+        gathered = [torch.empty(length, dtype=td).pin_memory() for _ in range(n)]
+        torch.cuda.synchronize()
+        ra.ra_allgather(shards, gathered)
+        torch.cuda.synchronize()
+        for r in range(n):
+            assert_same_bits(to_host(host_out[r], dtype), want[r], dtype, f"AR host->host n={n} rank {r}")
+            assert_same_bits(to_host(dev_out[r], dtype), want[r], dtype, f"AR host->device n={n} rank {r}")
+            assert_same_bits(to_host(shards[r], dtype), shards_want[r], dtype, f"RS host n={n} shard {r}")
+            assert_same_bits(to_host(gathered[r], dtype), want[r], dtype, f"AG host n={n} rank {r}")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        with pytest.raises(ra.RaError, match="unsupported"):
+            ra.ra_allreduce_ex(sends, host_out, "avg", engine="bulk", status=status)
+        with pytest.raises(ra.RaError, match="unsupported"):
+            ra.ra_allreduce_ex(sends, host_out, "avg", order="tree")
+        torch.cuda.synchronize()
+        assert status.item() == 0
+
+
 @pytest.mark.parametrize("n", [3, 5, 12])
 def test_allgather_mixed_phases(ra, n):
     # destinations at different element offsets share no vector grid, so every element takes the
