@@ -316,6 +316,15 @@ def test_pinned_host_buffers(ra, dtype):
             assert_same_bits(to_host(dev_out[r], dtype), want[r], dtype, f"AR host->device n={n} rank {r}")
             assert_same_bits(to_host(shards[r], dtype), shards_want[r], dtype, f"RS host n={n} shard {r}")
             assert_same_bits(to_host(gathered[r], dtype), want[r], dtype, f"AG host n={n} rank {r}")
+        # DDP-style buckets on the same host buffers: grouped launches, each bucket its own all-reduce
+        plan = ra.ra_bucket_plan([length // 3, length // 3, length - 2 * (length // 3)], 4096, ELEM_SIZE[dtype])
+        bucket_out = [torch.empty(length, dtype=td).pin_memory() for _ in range(n)]
+        ra.ra_allreduce_buckets(sends, bucket_out, plan, "avg")
+        torch.cuda.synchronize()
+        for b, c in plan:
+            bw, _, _ = oracle.allreduce([np.ascontiguousarray(x[b:b + c]) for x in xs], "avg", dtype)
+            for r in range(n):
+                assert_same_bits(to_host(bucket_out[r][b:b + c], dtype), bw[r], dtype, f"bucket {b}+{c} n={n} rank {r}")
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         with pytest.raises(ra.RaError, match="unsupported"):
             ra.ra_allreduce_ex(sends, host_out, "avg", engine="bulk", status=status)
