@@ -507,6 +507,9 @@ int trip_shape_for(int kind, int nranks, int elem_bytes, bool acc32, bool minmax
   // points at every size)
   if (rs && offgrid && elem_bytes == 2 && !minmax && nranks >= 5 && nranks <= 7 && total_bytes >= (320ull << 20))
     return ra::SHAPE_TRIP_W_OFFGRID;
+  // fp32 partials take a trip from N = 3 when every shard is on the vector grid (TripAccRS: +0.6-3.8
+  // points at 256 MiB - 1 GiB over all ranks against one wave)
+  if (rs && acc32 && shards_on_grid && nranks >= 3) return trip;
   if (rs) return (nranks >= 8 || (elem_bytes == 4 && nranks >= 4)) ? trip : -1;
   return nranks >= 3 ? trip : -1;
 #endif

@@ -152,8 +152,8 @@ using ShapeW8 = ShapeS;
 // 96-100%), 91-98% at 128 MiB (85-94%); reduce-scatter from N = 8 104-107%
 // (100-104%), min/max on 128 x 2 at 4 CTAs/SM.
 // fp32 partials take TripS for the all-reduce (bf16 avg: 102.5-104.8% at 1 GiB,
-// N = 3..16, against 95.9-99.5% one-wave) and TripRS2 for the reduce-scatter
-// (101.9 / 103.3% at N = 8 / 16 against 96.1 / 98.4%; TripS would spill there).
+// N = 3..16, against 95.9-99.5% one-wave) and TripAccRS (below) for the
+// reduce-scatter (TripS, with loads of 4 ranks, would spill there).
 using TripS = Shape<128, 8, 1, 4>;
 using TripRS2 = Shape<128, 4, 2, 4>;
 // N <= 2 has too few loads per thread on TripS to keep HBM busy; 128 x 2 at 8
@@ -166,6 +166,13 @@ using TripRS2 = Shape<128, 4, 2, 4>;
 // with every shard on the grid, reduce-scatters take it up to N = 4, and up to
 // N = 7 for 16-bit types and float min/max (106-108.7% at 1 GiB).
 using TripW = Shape<128, 8, 2, 2>;
+// fp32 partials in the reduce-scatter: 128 x 1 at 8 CTAs/SM with loads of 2
+// ranks (bf16 avg, shards on the vector grid, N = 3..16): 100.4-103.9% at 1 GiB
+// over all ranks, 94.5-95.6% at 256 MiB and 86.6-89.1% at 128 MiB from N = 6,
+// against 98.9-103.8%, 76.7-96.7% and 79.7-91.8% on TripRS2 (128 x 2 at 4
+// CTAs/SM, loads of 4 ranks); 128 x 2 at 4 CTAs/SM with loads of 2 measured
+// between the two.
+using TripAccRS = Shape<128, 8, 1, 2>;
 // SHAPE_RS_OFFGRID(_B2, _M): a reduce-scatter with some compact output off the
 // vector grid at a 2-byte offset, on ShapeS, or on ShapeRS2 (where the plain
 // call would take loads of 2 ranks at a time; _M: with fp32 partials).
@@ -188,7 +195,7 @@ enum ShapeId {
   SHAPE_TRIP_S = 15,    // TripS, one trip per CTA (all-reduce; reduce-scatter sum/avg/prod)
   SHAPE_TRIP_RS2 = 16,  // TripRS2, one trip per CTA (reduce-scatter min/max)
   SHAPE_TRIP_ACC = 17,  // TripS, one trip per CTA, fp32 partials (all-reduce)
-  SHAPE_TRIP_ACC_RS2 = 18,  // TripRS2, one trip per CTA, fp32 partials (reduce-scatter)
+  SHAPE_TRIP_ACC_RS2 = 18,  // TripAccRS, one trip per CTA, fp32 partials (reduce-scatter)
   SHAPE_TRIP_RS_OFFGRID = 19,  // TripS, one trip per CTA, reduce-scatter with 2-byte-offset shards
   SHAPE_TRIP_W = 20,           // TripW, one trip per CTA (small N)
   SHAPE_TRIP_RS2_OFFGRID = 21,  // TripRS2, one trip per CTA, min/max reduce-scatter with 2-byte-offset shards
@@ -803,7 +810,7 @@ cudaError_t launch_fused(int kind, const Args& a, dim3 grid, cudaStream_t s) {
       break;
     case SHAPE_TRIP_ACC_RS2:
       if constexpr (ACC32) {
-        if (rs) return launch_rs<DT, OP, true, TripRS2, false, true>(a, grid, s);
+        if (rs) return launch_rs<DT, OP, true, TripAccRS, false, true>(a, grid, s);
       }
       break;
     case SHAPE_TRIP_RS_OFFGRID:
@@ -867,7 +874,7 @@ inline void shape_params(int shape, int* threads, int* unroll, int* min_blocks) 
     case SHAPE_TRIP_S: return shape_params_of<TripS>(threads, unroll, min_blocks);
     case SHAPE_TRIP_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
     case SHAPE_TRIP_ACC: return shape_params_of<TripS>(threads, unroll, min_blocks);
-    case SHAPE_TRIP_ACC_RS2: return shape_params_of<TripRS2>(threads, unroll, min_blocks);
+    case SHAPE_TRIP_ACC_RS2: return shape_params_of<TripAccRS>(threads, unroll, min_blocks);
     case SHAPE_TRIP_RS_OFFGRID: return shape_params_of<TripS>(threads, unroll, min_blocks);
     case SHAPE_TRIP_W: return shape_params_of<TripW>(threads, unroll, min_blocks);
     case SHAPE_TRIP_RS2_OFFGRID: return shape_params_of<TripRS2>(threads, unroll, min_blocks);

@@ -753,8 +753,11 @@ def _run_ex(ra, xs, op, dtype, order="ring", accum="dtype"):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("op", OPS)
 def test_fp32_accumulation(ra, dtype, op):
+    # ragged lengths, and lengths whose shards all sit on the vector grid (the reduce-scatter then takes
+    # a CTA per trip from N = 3)
     for n, length in ((1, 100), (2, 1001), (3, 4097), (6, 6 * 4099 + 5), (7, 30_011), (8, 65536 + 5), (16, 1003),
-                      (64, 64 * 33 + 1)):
+                      (64, 64 * 33 + 1), (3, 3 * 16 * 300), (4, 4 * 16 * 257), (5, 5 * 16 * 300), (7, 7 * 16 * 250),
+                      (12, 12 * 16 * 100)):
         xs = inputs.rank_buffers(n, length, dtype, dist_for(dtype, op), seed_base=n + 17)
         want, _ = oracle.allreduce_ex(xs, op, dtype, accum="fp32")
         got, shards = _run_ex(ra, xs, op, dtype, accum="fp32")
