@@ -471,7 +471,8 @@ ra_status_t run_ordered(int kind, const ra::Args& a, int dtype, int op, int orde
 //   on and off the grid (bf16 with 2-byte-offset shards, N = 9..15: 102.3-104.5%
 //   against 94.6-100.3% on TripS);
 // - fp32 partials and shards off the vector grid take trips too, but not both
-//   at once (bf16 avg at N = 12: 96.7% one-wave against 90.0%);
+//   at once (bf16 avg at N = 12: 96.7% one-wave against 90.0%); reduce-scatters
+//   with fp32 partials from N = 3 when every shard is on the grid (TripAccRS);
 // - large 16-bit off-grid sums at N = 5..7 (below).
 // RA_GRID_MODE, a build-time tunable for sweeps: -1 these rules, 0 never, 1
 // wherever a trip shape exists.
